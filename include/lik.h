@@ -1,0 +1,178 @@
+/*
+ * lik.h -- C ABI of liblik, a GB300 (sm_103a) implementation of the
+ * late-interaction MaxSim operator.
+ *
+ * The operator (Late Interaction Kernels README, "What does it compute?"):
+ *
+ *     score(q, d) = sum over valid query tokens i of
+ *                   max over valid document tokens j of  Q[q,i,:] . D[d,j,:]
+ *
+ * Semantics shared by every entry point (README, "Scoring interface" and
+ * "Precision and compatibility"):
+ *   - Q and D share one dtype (fp32, fp16 or bf16) and one embedding size
+ *     `dim`; the library never normalises them (raw dot products).
+ *   - Masks are 1 byte per token (C `bool`, torch.bool): nonzero = valid,
+ *     0 = padding.  A NULL mask means every token is valid.  A query mask
+ *     removes token i from the sum; a document mask removes token j from the
+ *     max.
+ *   - A document with no valid token scores exactly -1e9, whatever the query.
+ *     A non-empty document scored against a query with no valid token
+ *     scores 0.
+ *   - Scores are fp32.  Similarities accumulate in fp32: fp16/bf16 inputs on
+ *     the tensor cores (tcgen05, fp32 accumulators), fp32 inputs with fp32
+ *     FMA (never TF32).
+ *   - argmax[..., i] is the document-token index j (0 <= j < Ld, counted
+ *     within its own document) whose similarity is the max for query token
+ *     i; the lowest such j on exact ties.  It is -1 for a masked query token
+ *     and for every token of an empty document.
+ *
+ * Backward (README, "What does it compute?": gradients flow into query and
+ * document embeddings; LIK announcement thread, post 5/N: the backward is
+ * fused).  The score is piecewise linear; with upstream gradient g per score
+ *     grad_Q[q,i,:] = sum over pairs (q,d) of g[q,d] * D[d, argmax[q,d,i], :]
+ *     grad_D[d,j,:] = sum over (q,i) with argmax[q,d,i] == j of g[q,d] * Q[q,i,:]
+ * Entries with argmax -1 contribute nothing, so grad_out of an empty
+ * document is ignored.  The backward reads the masks only through the
+ * argmax that the forward saved.
+ *
+ * Memory, ownership, streams:
+ *   - Every pointer is a device pointer (cudaMalloc or managed memory) of
+ *     the current device, row-major and contiguous.  Q and D must be 16-byte
+ *     aligned.  Host pointers are rejected with LIK_ERR_INVALID_ARG.
+ *   - The caller allocates every buffer, outputs included.  The library
+ *     allocates no device memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
+ *     Outputs are complete when the stream reaches the call.  Gradients are
+ *     overwritten, not accumulated into.
+ *   - Functions are thread-safe.
+ *
+ * Errors:
+ *   - LIK_ERR_INVALID_ARG: a negative size, a NULL required pointer, a host
+ *     pointer, a misaligned Q/D, an unknown dtype.  Nothing is launched.
+ *   - LIK_ERR_UNSUPPORTED: the current device is not sm_103 (GB300), or a
+ *     size is beyond the documented limits.  Nothing is launched.  There is
+ *     no fallback to another backend.
+ *   - LIK_ERR_CUDA: a CUDA call or launch failed; the CUDA error is
+ *     propagated, never swallowed (colpali PR "Add support for
+ *     late-interaction-kernels (LIK)", Design section: real kernel errors
+ *     always propagate).  lik_last_error_message() names it.
+ *   - LIK_ERR_TIMEOUT: reported by lik_check_device_error() when a kernel's
+ *     bounded pipeline wait expired; the kernel stopped and its outputs are
+ *     not valid.
+ *
+ * Sizes: 0 <= Nq, Nd, B, N; 0 <= Lq, Ld; 1 <= dim <= 1024.  Zero pairs is a
+ * no-op.  Ld == 0 makes every document empty (-1e9).  Lq == 0 gives 0 for
+ * every non-empty document.
+ */
+#ifndef LIK_H
+#define LIK_H
+
+#include <stdbool.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LIK_F32 = 0,
+    LIK_F16 = 1,
+    LIK_BF16 = 2
+} lik_dtype;
+
+typedef enum {
+    LIK_OK = 0,
+    LIK_ERR_INVALID_ARG = 1,
+    LIK_ERR_UNSUPPORTED = 2,
+    LIK_ERR_CUDA = 3,
+    LIK_ERR_TIMEOUT = 4
+} lik_status;
+
+/* Static, never-NULL description of a status code. */
+const char* lik_status_string(lik_status status);
+
+/* Human-readable detail of the last non-OK status returned on the calling
+ * host thread ("" if none).  Valid until the next call on that thread. */
+const char* lik_last_error_message(void);
+
+/* Library version string, e.g. "0.1.0". */
+const char* lik_version(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device-side error word
+ * that kernels set when a bounded wait expires.  Returns LIK_ERR_TIMEOUT if
+ * it was set, LIK_ERR_CUDA if the stream reported a CUDA error, LIK_OK
+ * otherwise.  This is the only entry point that blocks the host.
+ */
+lik_status lik_check_device_error(cudaStream_t stream);
+
+/* ------------------------------------------------------------ all-pairs --
+ * README "Scoring interface" table, layer MaxSim: every query against every
+ * document ("for example for in-batch training").
+ *   Q      [Nq, Lq, dim]   dtype
+ *   D      [Nd, Ld, dim]   dtype
+ *   qmask  [Nq, Lq]        or NULL
+ *   dmask  [Nd, Ld]        or NULL
+ *   scores [Nq, Nd]        fp32, written
+ *   argmax [Nq, Nd, Lq]    int32, written; NULL for inference (no backward)
+ */
+lik_status lik_maxsim_allpairs_fwd(const void* Q, const void* D, lik_dtype dtype,
+                                   int64_t Nq, int64_t Nd, int64_t Lq, int64_t Ld,
+                                   int64_t dim, const bool* qmask, const bool* dmask,
+                                   float* scores, int32_t* argmax, cudaStream_t stream);
+
+/*
+ *   grad_out [Nq, Nd]        fp32
+ *   argmax   [Nq, Nd, Lq]    int32, as written by lik_maxsim_allpairs_fwd
+ *   grad_Q   [Nq, Lq, dim]   fp32, overwritten; NULL to skip
+ *   grad_D   [Nd, Ld, dim]   fp32, overwritten; NULL to skip
+ */
+lik_status lik_maxsim_allpairs_bwd(const void* Q, const void* D, lik_dtype dtype,
+                                   int64_t Nq, int64_t Nd, int64_t Lq, int64_t Ld,
+                                   int64_t dim, const float* grad_out,
+                                   const int32_t* argmax, float* grad_Q, float* grad_D,
+                                   cudaStream_t stream);
+
+/* ------------------------------------------------------------- pairwise --
+ * README "Scoring interface" table, layer MaxSimPairwise: query b against
+ * document b only ("for reranking, without computing the full cross
+ * product").
+ *   Q [B, Lq, dim], D [B, Ld, dim], qmask [B, Lq], dmask [B, Ld],
+ *   scores [B], argmax [B, Lq] (or NULL)
+ */
+lik_status lik_maxsim_pairwise_fwd(const void* Q, const void* D, lik_dtype dtype,
+                                   int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
+                                   const bool* qmask, const bool* dmask,
+                                   float* scores, int32_t* argmax, cudaStream_t stream);
+
+/*   grad_out [B], argmax [B, Lq], grad_Q [B, Lq, dim], grad_D [B, Ld, dim] */
+lik_status lik_maxsim_pairwise_bwd(const void* Q, const void* D, lik_dtype dtype,
+                                   int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
+                                   const float* grad_out, const int32_t* argmax,
+                                   float* grad_Q, float* grad_D, cudaStream_t stream);
+
+/* ------------------------------------------------- per-query candidates --
+ * colpali PR "Add support for late-interaction-kernels (LIK)", Design
+ * section (maxsim_kd, the per-query candidate layout used by the
+ * negative-document losses): query b against its own N candidates.
+ *   Q [B, Lq, dim], D [B, N, Ld, dim], qmask [B, Lq], dmask [B, N, Ld],
+ *   scores [B, N], argmax [B, N, Lq] (or NULL)
+ */
+lik_status lik_maxsim_kd_fwd(const void* Q, const void* D, lik_dtype dtype,
+                             int64_t B, int64_t N, int64_t Lq, int64_t Ld, int64_t dim,
+                             const bool* qmask, const bool* dmask,
+                             float* scores, int32_t* argmax, cudaStream_t stream);
+
+/*   grad_out [B, N], argmax [B, N, Lq], grad_Q [B, Lq, dim], grad_D [B, N, Ld, dim] */
+lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype,
+                             int64_t B, int64_t N, int64_t Lq, int64_t Ld, int64_t dim,
+                             const float* grad_out, const int32_t* argmax,
+                             float* grad_Q, float* grad_D, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIK_H */

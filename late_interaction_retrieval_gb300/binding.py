@@ -1,0 +1,223 @@
+"""Thin ctypes binding of liblik (C ABI: include/lik.h).
+
+Argument marshalling only: each function checks that the torch tensors have
+the shapes, dtypes and device the C ABI expects, passes their device
+pointers and the current CUDA stream, and raises :class:`LIKError` on a
+non-OK status.  Every step of the operator runs in liblik's kernels; there
+is no other backend and no CPU fallback.  If liblik cannot be loaded (not
+built, or built for another machine) the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+LIK_F32, LIK_F16, LIK_BF16 = 0, 1, 2
+STATUS = {0: "LIK_OK", 1: "LIK_ERR_INVALID_ARG", 2: "LIK_ERR_UNSUPPORTED", 3: "LIK_ERR_CUDA",
+          4: "LIK_ERR_TIMEOUT"}
+
+# Every entry point include/lik.h declares, with its ctypes signature.
+_P, _I64, _I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+SIGNATURES = {
+    "lik_status_string": (ctypes.c_char_p, [_I32]),
+    "lik_last_error_message": (ctypes.c_char_p, []),
+    "lik_version": (ctypes.c_char_p, []),
+    "lik_check_device_error": (_I32, [_P]),
+    "lik_maxsim_allpairs_fwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_allpairs_bwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_pairwise_fwd": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
+    "lik_maxsim_pairwise_bwd": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
+    "lik_maxsim_kd_fwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_kd_bwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+}
+
+_DTYPES = {torch.float32: LIK_F32, torch.float16: LIK_F16, torch.bfloat16: LIK_BF16}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LIKError(RuntimeError):
+    """A liblik call returned a non-OK status."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS.get(status, f"status {status}")
+        super().__init__(f"{self.status_name}: {message}")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load liblik (building it first if it is missing or stale and nvcc exists)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or library_path()
+        if path is None and not _build.up_to_date():
+            try:
+                _build.build()
+            except Exception as e:  # the CUDA path is the only path: say so loudly
+                raise RuntimeError(f"liblik is not built and the build failed: {e}") from e
+        if not os.path.exists(p):
+            raise RuntimeError(f"liblik not found at {p}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != 0:
+        msg = load().lik_last_error_message().decode()
+        raise LIKError(status, msg)
+
+
+def _stream(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _need(t: torch.Tensor | None, name: str, shape, dtype, device, optional=False):
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _embeddings(Q: torch.Tensor, D: torch.Tensor, q_rank: int, d_rank: int):
+    if Q.dim() != q_rank or D.dim() != d_rank:
+        raise ValueError(f"expected Q of rank {q_rank} and D of rank {d_rank}")
+    if Q.dtype != D.dtype or Q.dtype not in _DTYPES:
+        raise ValueError(f"Q and D must share one dtype of float32/float16/bfloat16 "
+                         f"(got {Q.dtype}, {D.dtype})")
+    if Q.device != D.device or Q.device.type != "cuda":
+        raise ValueError("Q and D must be CUDA tensors on one device")
+    if Q.shape[-1] != D.shape[-1]:
+        raise ValueError("Q and D must share the embedding dimension")
+    if not (Q.is_contiguous() and D.is_contiguous()):
+        raise ValueError("Q and D must be contiguous")
+    return _DTYPES[Q.dtype], Q.device
+
+
+# ----------------------------------------------------------- all-pairs --
+
+def lik_maxsim_allpairs_fwd(Q, D, qmask, dmask, scores, argmax=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    _need(qmask, "qmask", (Nq, Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", (Nd, Ld), torch.bool, dev, optional=True)
+    _need(scores, "scores", (Nq, Nd), torch.float32, dev)
+    _need(argmax, "argmax", (Nq, Nd, Lq), torch.int32, dev, optional=True)
+    _check(load().lik_maxsim_allpairs_fwd(
+        _ptr(Q), _ptr(D), dt, Nq, Nd, Lq, Ld, dim, _ptr(qmask), _ptr(dmask),
+        _ptr(scores), _ptr(argmax), _stream(dev, stream)))
+
+
+def lik_maxsim_allpairs_bwd(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    _need(grad_out, "grad_out", (Nq, Nd), torch.float32, dev)
+    _need(argmax, "argmax", (Nq, Nd, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (Nq, Lq, dim), torch.float32, dev, optional=True)
+    _need(grad_D, "grad_D", (Nd, Ld, dim), torch.float32, dev, optional=True)
+    _check(load().lik_maxsim_allpairs_bwd(
+        _ptr(Q), _ptr(D), dt, Nq, Nd, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+# ------------------------------------------------------------ pairwise --
+
+def lik_maxsim_pairwise_fwd(Q, D, qmask, dmask, scores, argmax=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    B, Lq, dim = Q.shape
+    if D.shape[0] != B:
+        raise ValueError("pairwise: Q and D must have the same batch size")
+    Ld = D.shape[1]
+    _need(qmask, "qmask", (B, Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", (B, Ld), torch.bool, dev, optional=True)
+    _need(scores, "scores", (B,), torch.float32, dev)
+    _need(argmax, "argmax", (B, Lq), torch.int32, dev, optional=True)
+    _check(load().lik_maxsim_pairwise_fwd(
+        _ptr(Q), _ptr(D), dt, B, Lq, Ld, dim, _ptr(qmask), _ptr(dmask),
+        _ptr(scores), _ptr(argmax), _stream(dev, stream)))
+
+
+def lik_maxsim_pairwise_bwd(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    B, Lq, dim = Q.shape
+    Ld = D.shape[1]
+    _need(grad_out, "grad_out", (B,), torch.float32, dev)
+    _need(argmax, "argmax", (B, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (B, Lq, dim), torch.float32, dev, optional=True)
+    _need(grad_D, "grad_D", (B, Ld, dim), torch.float32, dev, optional=True)
+    _check(load().lik_maxsim_pairwise_bwd(
+        _ptr(Q), _ptr(D), dt, B, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+# ------------------------------------------------- per-query candidates --
+
+def lik_maxsim_kd_fwd(Q, D, qmask, dmask, scores, argmax=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 4)
+    B, Lq, dim = Q.shape
+    if D.shape[0] != B:
+        raise ValueError("kd: Q and D must have the same batch size")
+    N, Ld = D.shape[1], D.shape[2]
+    _need(qmask, "qmask", (B, Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", (B, N, Ld), torch.bool, dev, optional=True)
+    _need(scores, "scores", (B, N), torch.float32, dev)
+    _need(argmax, "argmax", (B, N, Lq), torch.int32, dev, optional=True)
+    _check(load().lik_maxsim_kd_fwd(
+        _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(qmask), _ptr(dmask),
+        _ptr(scores), _ptr(argmax), _stream(dev, stream)))
+
+
+def lik_maxsim_kd_bwd(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 4)
+    B, Lq, dim = Q.shape
+    N, Ld = D.shape[1], D.shape[2]
+    _need(grad_out, "grad_out", (B, N), torch.float32, dev)
+    _need(argmax, "argmax", (B, N, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (B, Lq, dim), torch.float32, dev, optional=True)
+    _need(grad_D, "grad_D", (B, N, Ld, dim), torch.float32, dev, optional=True)
+    _check(load().lik_maxsim_kd_bwd(
+        _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+def lik_check_device_error(stream=None, device=None):
+    """Synchronise the stream and raise if a kernel flagged an error."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(load().lik_check_device_error(_stream(dev, stream)))
+
+
+def version() -> str:
+    return load().lik_version().decode()

@@ -1,0 +1,354 @@
+// api.cu -- the C ABI of liblik (declared in include/lik.h): argument
+// validation, kernel selection and error propagation.
+//
+// Validation mirrors the eligibility checks the colpali PR "Add support for
+// late-interaction-kernels (LIK)" describes for its backend (Design section:
+// device capability, embedding size, matching devices), with one difference:
+// an ineligible call returns a status code and never falls back to another
+// backend.  CUDA errors are always propagated (same section: real kernel
+// errors always propagate).
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "lik.h"
+#include "lik_internal.h"
+
+namespace lik {
+
+// ---------------------------------------------------------- device state --
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceSlot {
+    std::once_flag once;
+    DeviceInfo info;
+    cudaError_t init_error = cudaSuccess;
+};
+DeviceSlot g_devices[kMaxDevices];
+
+// Set by kernels whose bounded waits expire or that meet an invalid saved
+// argmax; read and cleared by lik_check_device_error().
+__device__ unsigned int g_error_word;
+
+struct ErrorWordSlot {
+    std::once_flag once;
+    unsigned int* ptr = nullptr;
+};
+ErrorWordSlot g_error_words[kMaxDevices];
+
+thread_local char t_message[512];
+
+lik_status fail(lik_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_message, sizeof t_message, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+lik_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(LIK_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+}  // namespace
+
+const DeviceInfo& device_info(int device) {
+    DeviceSlot& slot = g_devices[device % kMaxDevices];
+    std::call_once(slot.once, [&] {
+        DeviceInfo& d = slot.info;
+        d.device = device;
+        cudaError_t e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, device);
+        if (e == cudaSuccess)
+            e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+        slot.init_error = e;
+    });
+    return slot.info;
+}
+
+unsigned int* device_error_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    ErrorWordSlot& slot = g_error_words[dev % kMaxDevices];
+    std::call_once(slot.once, [&] {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_error_word) == cudaSuccess)
+            slot.ptr = static_cast<unsigned int*>(p);
+    });
+    return slot.ptr;
+}
+
+// ------------------------------------------------------------ validation --
+
+namespace {
+
+bool known_dtype(lik_dtype t) { return t == LIK_F32 || t == LIK_F16 || t == LIK_BF16; }
+
+// The current device must be a GB300 (sm_103): the kernels are built for
+// sm_103a only.
+lik_status check_device(int* dev_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const DeviceInfo& info = device_info(dev);
+    if (g_devices[dev % kMaxDevices].init_error != cudaSuccess)
+        return cuda_fail(g_devices[dev % kMaxDevices].init_error, "cudaDeviceGetAttribute");
+    if (info.major != 10 || info.minor != 3)
+        return fail(LIK_ERR_UNSUPPORTED, "device %d is sm_%d%d; liblik is built for sm_103a (GB300)",
+                    dev, info.major, info.minor);
+    if (!device_error_word()) return fail(LIK_ERR_CUDA, "cannot resolve the device error word");
+    *dev_out = dev;
+    return LIK_OK;
+}
+
+// A non-NULL pointer must be device (or managed) memory of device `dev`.
+lik_status check_pointer(const void* p, int dev, const char* name) {
+    if (!p) return LIK_OK;
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+        return fail(LIK_ERR_INVALID_ARG, "%s is not a CUDA pointer", name);
+    }
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+        return fail(LIK_ERR_INVALID_ARG, "%s is not device memory", name);
+    if (attr.device != dev)
+        return fail(LIK_ERR_INVALID_ARG, "%s lives on device %d, current device is %d", name,
+                    attr.device, dev);
+    return LIK_OK;
+}
+
+struct Spec {
+    const char* name;
+    const void* ptr;
+    bool required;  // must be non-NULL when the buffer has elements
+    int64_t elems;
+};
+
+lik_status check_common(lik_dtype dtype, int64_t n_query, int64_t n_doc, int64_t ppq,
+                        int64_t Lq, int64_t Ld, int64_t dim, bool* nothing_to_do) {
+    *nothing_to_do = false;
+    if (!known_dtype(dtype)) return fail(LIK_ERR_INVALID_ARG, "unknown dtype %d", (int)dtype);
+    if (n_query < 0 || n_doc < 0 || ppq < 0 || Lq < 0 || Ld < 0)
+        return fail(LIK_ERR_INVALID_ARG, "negative size");
+    if (dim < 1) return fail(LIK_ERR_INVALID_ARG, "dim must be >= 1 (got %lld)", (long long)dim);
+    if (dim > 1024) return fail(LIK_ERR_UNSUPPORTED, "dim %lld > 1024", (long long)dim);
+    if (Lq > 4096) return fail(LIK_ERR_UNSUPPORTED, "Lq %lld > 4096", (long long)Lq);
+    if (Ld > (int64_t(1) << 30)) return fail(LIK_ERR_UNSUPPORTED, "Ld %lld > 2^30", (long long)Ld);
+    *nothing_to_do = (n_query == 0 || ppq == 0);
+    return LIK_OK;
+}
+
+lik_status check_buffers(int dev, const Spec* specs, int n) {
+    for (int k = 0; k < n; ++k) {
+        const Spec& s = specs[k];
+        if (s.required && s.elems > 0 && !s.ptr) return fail(LIK_ERR_INVALID_ARG, "%s is NULL", s.name);
+        if (s.elems > 0) {
+            lik_status st = check_pointer(s.ptr, dev, s.name);
+            if (st != LIK_OK) return st;
+        }
+    }
+    return LIK_OK;
+}
+
+lik_status check_alignment(const void* Q, const void* D) {
+    if ((reinterpret_cast<uintptr_t>(Q) & 15) || (reinterpret_cast<uintptr_t>(D) & 15))
+        return fail(LIK_ERR_INVALID_ARG, "Q and D must be 16-byte aligned");
+    return LIK_OK;
+}
+
+Problem make_problem(int layout, lik_dtype dtype, const void* Q, const void* D,
+                     const bool* qmask, const bool* dmask, int64_t n_query, int64_t n_doc,
+                     int64_t ppq, int64_t n_pairs, int64_t Lq, int64_t Ld, int64_t dim) {
+    Problem P;
+    P.layout = layout;
+    P.dtype = static_cast<int>(dtype);
+    P.Q = Q;
+    P.D = D;
+    P.qmask = reinterpret_cast<const uint8_t*>(qmask);
+    P.dmask = reinterpret_cast<const uint8_t*>(dmask);
+    P.n_query = n_query;
+    P.n_doc = n_doc;
+    P.pairs_per_query = ppq;
+    P.n_pairs = n_pairs;
+    P.Lq = Lq;
+    P.Ld = Ld;
+    P.dim = dim;
+    return P;
+}
+
+lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float* scores,
+                   int32_t* argmax, cudaStream_t stream) {
+    int dev = 0;
+    lik_status st = check_device(&dev);
+    if (st != LIK_OK) return st;
+    const int64_t q_elems = P.n_query * P.Lq * P.dim, d_elems = P.n_doc * P.Ld * P.dim;
+    const Spec specs[] = {
+        {"Q", P.Q, true, q_elems},
+        {"D", P.D, true, d_elems},
+        {"qmask", qmask, false, P.n_query * P.Lq},
+        {"dmask", dmask, false, P.n_doc * P.Ld},
+        {"scores", scores, true, P.n_pairs},
+        {"argmax", argmax, false, P.n_pairs * P.Lq},
+    };
+    if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
+    if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
+    const bool tc = tc_allpairs_eligible(P);
+    cudaError_t e = tc ? launch_fwd_tc_allpairs(P, scores, argmax, stream)
+                       : launch_fwd_simt(P, scores, argmax, stream);
+    if (e != cudaSuccess) return cuda_fail(e, tc ? "tensor-core forward launch" : "forward launch");
+    return LIK_OK;
+}
+
+lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argmax, float* grad_Q,
+                   float* grad_D, cudaStream_t stream) {
+    int dev = 0;
+    lik_status st = check_device(&dev);
+    if (st != LIK_OK) return st;
+    const int64_t q_elems = P.n_query * P.Lq * P.dim, d_elems = P.n_doc * P.Ld * P.dim;
+    const bool need_hits = P.n_pairs * P.Lq > 0 && (grad_Q || grad_D);
+    if (need_hits && !argmax) return fail(LIK_ERR_INVALID_ARG, "argmax is NULL");
+    if (need_hits && !grad_out) return fail(LIK_ERR_INVALID_ARG, "grad_out is NULL");
+    const Spec specs[] = {
+        {"Q", P.Q, grad_D != nullptr, q_elems},
+        {"D", P.D, grad_Q != nullptr, d_elems},
+        {"grad_out", grad_out, false, P.n_pairs},
+        {"argmax", argmax, false, P.n_pairs * P.Lq},
+        {"grad_Q", grad_Q, false, q_elems},
+        {"grad_D", grad_D, false, d_elems},
+    };
+    if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
+    if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
+    cudaError_t e;
+    if (grad_Q && (e = launch_bwd_grad_q(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess)
+        return cuda_fail(e, "grad_Q launch");
+    if (grad_D && (e = launch_bwd_grad_d(P, grad_out, argmax, grad_D, stream)) != cudaSuccess)
+        return cuda_fail(e, "grad_D launch");
+    return LIK_OK;
+}
+
+}  // namespace
+}  // namespace lik
+
+using namespace lik;
+
+// ================================================================ C ABI ===
+
+extern "C" {
+
+const char* lik_status_string(lik_status s) {
+    switch (s) {
+    case LIK_OK: return "LIK_OK";
+    case LIK_ERR_INVALID_ARG: return "LIK_ERR_INVALID_ARG";
+    case LIK_ERR_UNSUPPORTED: return "LIK_ERR_UNSUPPORTED";
+    case LIK_ERR_CUDA: return "LIK_ERR_CUDA";
+    case LIK_ERR_TIMEOUT: return "LIK_ERR_TIMEOUT";
+    default: return "LIK_ERR_UNKNOWN_STATUS";
+    }
+}
+
+const char* lik_last_error_message(void) { return t_message; }
+
+const char* lik_version(void) { return "0.1.0"; }
+
+lik_status lik_check_device_error(cudaStream_t stream) {
+    t_message[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    unsigned int* w = device_error_word();
+    if (!w) return fail(LIK_ERR_CUDA, "cannot resolve the device error word");
+    unsigned int word = 0;
+    e = cudaMemcpy(&word, w, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word) {
+        const unsigned int zero = 0;
+        e = cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    }
+    if (word & kErrTimeout) return fail(LIK_ERR_TIMEOUT, "a kernel's bounded wait expired");
+    if (word & kErrBadIndex)
+        return fail(LIK_ERR_INVALID_ARG, "a saved argmax held an index >= Ld (entries skipped)");
+    return LIK_OK;
+}
+
+lik_status lik_maxsim_allpairs_fwd(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
+                                   int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,
+                                   const bool* qmask, const bool* dmask, float* scores,
+                                   int32_t* argmax, cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, Nq, Nd, Nd, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+    return run_fwd(P, qmask, dmask, scores, argmax, stream);
+}
+
+lik_status lik_maxsim_allpairs_bwd(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
+                                   int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,
+                                   const float* grad_out, const int32_t* argmax, float* grad_Q,
+                                   float* grad_D, cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, Nq, Nd, Nd, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kAllPairs, dtype, Q, D, nullptr, nullptr, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+    // With no pairs the gradients are still defined: all zeros.
+    if (nothing) P.n_pairs = 0;
+    return run_bwd(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_pairwise_fwd(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                   int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                   const bool* dmask, float* scores, int32_t* argmax,
+                                   cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kPairwise, dtype, Q, D, qmask, dmask, B, B, 1, B, Lq, Ld, dim);
+    return run_fwd(P, qmask, dmask, scores, argmax, stream);
+}
+
+lik_status lik_maxsim_pairwise_bwd(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                   int64_t Lq, int64_t Ld, int64_t dim, const float* grad_out,
+                                   const int32_t* argmax, float* grad_Q, float* grad_D,
+                                   cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kPairwise, dtype, Q, D, nullptr, nullptr, B, B, 1, B, Lq, Ld, dim);
+    return run_bwd(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_kd_fwd(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                             int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                             const bool* dmask, float* scores, int32_t* argmax,
+                             cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kKd, dtype, Q, D, qmask, dmask, B, B * N, N, B * N, Lq, Ld, dim);
+    return run_fwd(P, qmask, dmask, scores, argmax, stream);
+}
+
+lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                             int64_t Lq, int64_t Ld, int64_t dim, const float* grad_out,
+                             const int32_t* argmax, float* grad_Q, float* grad_D,
+                             cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kKd, dtype, Q, D, nullptr, nullptr, B, B * N, N, B * N, Lq, Ld, dim);
+    if (nothing) P.n_pairs = 0;
+    return run_bwd(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+}  // extern "C"

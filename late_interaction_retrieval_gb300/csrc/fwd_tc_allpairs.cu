@@ -1,0 +1,477 @@
+// fwd_tc_allpairs.cu -- all-pairs MaxSim forward on the sm_103a tensor cores.
+//
+// What it computes (Late Interaction Kernels README, "What does it compute?"
+// and "Scoring interface"): for every query q and document d,
+//   score[q,d] = sum over valid i of max over valid j of Q[q,i].D[d,j]
+// with the lowest j reaching each max saved as argmax, -1e9 for documents
+// with no valid token.  The similarity grid is never written anywhere: it
+// lives one tile at a time in tensor memory (LIK announcement thread, post
+// 4/N: stream document tiles through on-chip memory and keep a running max;
+// the design below is our own).
+//
+// Tiling.  Q is viewed as [Nq*Lq, dim]: a row block holds floor(128/Lq)
+// whole queries (128 accumulator rows, one query token per row).  D is
+// viewed as [Nd, Ld, dim]; every document is cut into tiles of T <= 256
+// tokens that start at its first token, so a tile never straddles two
+// documents (the last tile's columns past Ld are zero-filled by TMA and
+// masked).  One tile is the MMA
+//     S[128, T] = Qblock[128, dim] . Dtile[T, dim]^T      (fp32 in TMEM)
+// issued as dim/16 tcgen05.mma (kind::f16, M=128, N=T, K=16).
+//
+// Warp roles (320 threads, one CTA per SM, persistent over work units):
+//   warp 0      TMA producer: Q row blocks (2 buffers) and D tiles (S stages)
+//   warp 1      TMEM allocator + single-thread MMA issuer
+//   warps 2..9  epilogue: two warpgroups; warp w reads TMEM lanes
+//               32*(w%4)..+31, i.e. one accumulator row per thread.  The
+//               warpgroups split each tile's 32-column chunks (even / odd),
+//               keep a running (max, argmax) per row, and merge at the end of
+//               every document.
+// The accumulator is double-buffered in TMEM (2 x 256 columns), so the MMA of
+// tile t+1 overlaps the epilogue of tile t.
+//
+// Epilogue per 32-column chunk: one tcgen05.ld, the document mask as a
+// warp-uniform 32-bit word (one ballot), a lowest-index tournament over the
+// 32 values, and a strictly-greater merge into the running max -- so ties go
+// to the lowest token index, as in the oracle.  At a document's end the
+// maxima of the valid query tokens are summed per query (fixed order) and
+// the score and argmax are written.
+//
+// Every mbarrier wait is bounded (ptx::mbar_wait); on expiry the kernel sets
+// the library's error word, drains its own TMA loads and MMAs, frees TMEM and
+// returns.
+#include <cfloat>
+
+#include "lik_internal.h"
+#include "sm100_ptx.cuh"
+#include "tmap.h"
+
+namespace lik {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kM = 128;              // accumulator rows (query tokens) per tile
+constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
+constexpr int kAtomElems = 64;
+constexpr int kMaxStages = 6;
+constexpr int kAccCols = 256;        // TMEM columns per accumulator buffer
+
+struct Params {
+    int64_t Nq, Nd, Lq, Ld;
+    int dim, atoms, T, tiles_per_doc, qpt, n_rb, dpu, stages;
+    int64_t n_units;
+    uint32_t idesc, q_bytes, d_bytes;
+    const uint8_t* qmask;
+    const uint8_t* dmask;
+    float* scores;
+    int32_t* argmax;
+    unsigned int* err;
+};
+
+// Barrier slots in the misc region.
+struct Bars {
+    uint64_t full_d[kMaxStages], empty_d[kMaxStages];
+    uint64_t full_q[2], empty_q[2];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t xchg[2];   // document-end exchange between the two epilogue warpgroups (256)
+    uint64_t qsum[2];   // per-query sums inside warpgroup 0 (128)
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    uint32_t pad;
+};
+
+struct Exchange {
+    float m[2][kM];
+    int a[2][kM];
+    uint32_t any[2][4];
+    float part[2][kM];  // per-row terms or per-warp partial sums
+};
+
+__device__ __forceinline__ int ksteps_of_atom(int dim, int a) {
+    const int rem = dim - a * kAtomElems;
+    return (rem >= kAtomElems ? kAtomElems : rem) / 16;
+}
+
+// Lowest-index argmax of n values (n = 16 or 32) by a tournament: pairs are
+// compared with a strict '>' so the left (lower) index wins ties.
+template <int N>
+__device__ __forceinline__ void tournament(const float (&v)[N], float& best, int& idx) {
+    float m[N / 2];
+    int k[N / 2];
+#pragma unroll
+    for (int t = 0; t < N / 2; ++t) {
+        const bool p = v[2 * t + 1] > v[2 * t];
+        m[t] = p ? v[2 * t + 1] : v[2 * t];
+        k[t] = 2 * t + (p ? 1 : 0);
+    }
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1) {
+#pragma unroll
+        for (int t = 0; t < w; ++t) {
+            const bool p = m[2 * t + 1] > m[2 * t];
+            m[t] = p ? m[2 * t + 1] : m[2 * t];
+            k[t] = p ? k[2 * t + 1] : k[2 * t];
+        }
+    }
+    best = m[0];
+    idx = k[0];
+}
+
+template <int N>
+__device__ __forceinline__ void chunk_best(uint32_t taddr, uint32_t mw, float& best, int& idx) {
+    uint32_t raw[N];
+    if constexpr (N == 32)
+        ptx::tmem_ld_32(taddr, raw);
+    else
+        ptx::tmem_ld_16(taddr, raw);
+    float v[N];
+    const uint32_t full = N == 32 ? 0xffffffffu : 0xffffu;
+    if ((mw & full) == full) {
+#pragma unroll
+        for (int t = 0; t < N; ++t) v[t] = __uint_as_float(raw[t]);
+    } else {
+#pragma unroll
+        for (int t = 0; t < N; ++t) v[t] = ((mw >> t) & 1u) ? __uint_as_float(raw[t]) : -INFINITY;
+    }
+    tournament<N>(v, best, idx);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmd,
+                       const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* qbuf = smem;                                   // 2 x q_bytes
+    uint8_t* dbuf = smem + 2 * p.q_bytes;                   // stages x d_bytes
+    Bars* bars = reinterpret_cast<Bars*>(dbuf + p.stages * p.d_bytes);
+    Exchange* xc = reinterpret_cast<Exchange*>(bars + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned int* err = p.err;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            ptx::mbar_init(ptx::smem_u32(&bars->full_d[s]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->empty_d[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), 8);
+            ptx::mbar_init(ptx::smem_u32(&bars->xchg[b]), 256);
+            ptx::mbar_init(ptx::smem_u32(&bars->qsum[b]), 128);
+        }
+        ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), 2 * kAccCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = bars->tmem_base;
+
+    const int64_t Lq = p.Lq, Ld = p.Ld;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            ptx::prefetch_tmap(&tmq);
+            ptx::prefetch_tmap(&tmd);
+            int s = 0, qb = 0;
+            uint32_t ph = 0, qph = 0;
+            uint32_t issued_d = 0, issued_q = 0;  // bit i: slot i holds an issued load
+            uint32_t last_ph_d = 0, last_ph_q = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+                const int rb = static_cast<int>(u % p.n_rb);
+                const int64_t d0 = (u / p.n_rb) * p.dpu;
+                const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
+                if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_q[qb]), qph ^ 1, err))) break;
+                const uint32_t fq = ptx::smem_u32(&bars->full_q[qb]);
+                ptx::mbar_arrive_expect_tx(fq, p.q_bytes);
+                const int32_t row0 = static_cast<int32_t>(static_cast<int64_t>(rb) * p.qpt * Lq);
+                for (int a = 0; a < p.atoms; ++a)
+                    ptx::tma_load_2d(ptx::smem_u32(qbuf + qb * p.q_bytes + a * kM * kAtomBytes), &tmq,
+                                     a * kAtomElems, row0, fq);
+                issued_q |= 1u << qb;
+                last_ph_q = (last_ph_q & ~(1u << qb)) | (qph << qb);
+                if (++qb == 2) { qb = 0; qph ^= 1; }
+                for (int64_t d = d0; ok && d < d1; ++d) {
+                    for (int t = 0; t < p.tiles_per_doc; ++t) {
+                        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_d[s]), ph ^ 1, err))) break;
+                        const uint32_t fd = ptx::smem_u32(&bars->full_d[s]);
+                        ptx::mbar_arrive_expect_tx(fd, p.d_bytes);
+                        for (int a = 0; a < p.atoms; ++a)
+                            ptx::tma_load_3d(ptx::smem_u32(dbuf + s * p.d_bytes + a * p.T * kAtomBytes),
+                                             &tmd, a * kAtomElems, t * p.T, static_cast<int32_t>(d), fd);
+                        issued_d |= 1u << s;
+                        last_ph_d = (last_ph_d & ~(1u << s)) | (ph << s);
+                        if (++s == p.stages) { s = 0; ph ^= 1; }
+                    }
+                }
+            }
+            // every issued load must land before the CTA may exit
+            for (int k = 0; k < p.stages; ++k)
+                if (issued_d & (1u << k))
+                    ptx::mbar_wait(ptx::smem_u32(&bars->full_d[k]), (last_ph_d >> k) & 1u, err);
+            for (int k = 0; k < 2; ++k)
+                if (issued_q & (1u << k))
+                    ptx::mbar_wait(ptx::smem_u32(&bars->full_q[k]), (last_ph_q >> k) & 1u, err);
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------- MMA --
+        if (lane == 0) {
+            int s = 0, qb = 0, ab = 0;
+            uint32_t ph = 0, qph = 0, aph = 0;
+            bool ok = true;
+            for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+                const int64_t d0 = (u / p.n_rb) * p.dpu;
+                const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
+                if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_q[qb]), qph, err))) break;
+                ptx::tc_fence_after();
+                const uint32_t qaddr = ptx::smem_u32(qbuf + qb * p.q_bytes);
+                for (int64_t d = d0; ok && d < d1; ++d) {
+                    for (int t = 0; t < p.tiles_per_doc; ++t) {
+                        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph, err))) break;
+                        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[ab]), aph ^ 1, err))) break;
+                        ptx::tc_fence_after();
+                        const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
+                        const uint32_t acc = tmem_base + ab * kAccCols;
+                        bool accumulate = false;
+                        for (int a = 0; a < p.atoms; ++a) {
+                            const int ks = ksteps_of_atom(p.dim, a);
+                            for (int kk = 0; kk < ks; ++kk) {
+                                const uint64_t ad = ptx::sw128_kmajor_desc(qaddr + a * kM * kAtomBytes + kk * 32);
+                                const uint64_t bd = ptx::sw128_kmajor_desc(daddr + a * p.T * kAtomBytes + kk * 32);
+                                ptx::mma_f16(acc, ad, bd, p.idesc, accumulate);
+                                accumulate = true;
+                            }
+                        }
+                        ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
+                        ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
+                        if (++s == p.stages) { s = 0; ph ^= 1; }
+                        if (++ab == 2) { ab = 0; aph ^= 1; }
+                    }
+                }
+                ptx::mma_commit(ptx::smem_u32(&bars->empty_q[qb]));
+                if (++qb == 2) { qb = 0; qph ^= 1; }
+            }
+            // all MMAs this thread issued complete before TMEM is released
+            ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
+            ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, err);
+        }
+    } else {
+        // ------------------------------------------------------ epilogue --
+        const int ew = warp - 2;            // 0..7
+        const int half = ew >> 2;           // warpgroup: even / odd chunks
+        const int quarter = warp & 3;       // TMEM lane quarter of this warp
+        const int r = quarter * 32 + lane;  // accumulator row of this thread
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int nchunks = (p.T + 31) >> 5;
+        const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
+        const int qloc = static_cast<int>(r / Lq);
+        const int i = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
+        int ab = 0, par = 0;
+        uint32_t aph = 0, xph0 = 0, xph1 = 0, sph0 = 0, sph1 = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+            const int rb = static_cast<int>(u % p.n_rb);
+            const int64_t d0 = (u / p.n_rb) * p.dpu;
+            const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
+            const int64_t q = static_cast<int64_t>(rb) * p.qpt + qloc;
+            const bool row_ok = r < qrows && q < p.Nq;
+            const bool qvalid = row_ok && (!p.qmask || p.qmask[q * Lq + i]);
+            for (int64_t d = d0; ok && d < d1; ++d) {
+                float m = -INFINITY;
+                int am = -1;
+                uint32_t any = 0;
+                const uint8_t* dm = p.dmask ? p.dmask + d * Ld : nullptr;
+                for (int t = 0; t < p.tiles_per_doc; ++t) {
+                    const int64_t jt = static_cast<int64_t>(t) * p.T;
+                    // mask words of this warpgroup's chunks, fetched before the accumulator is ready
+                    uint32_t mw[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = half + 2 * k;
+                        const int col = c * 32 + lane;
+                        const int64_t j = jt + col;
+                        const bool v = c < nchunks && col < p.T && j < Ld && (!dm || dm[j]);
+                        mw[k] = __ballot_sync(0xffffffffu, v);
+                    }
+                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = half + 2 * k;
+                        if (c >= nchunks || mw[k] == 0) continue;
+                        any |= mw[k];
+                        float cb;
+                        int ci;
+                        if (p.T - c * 32 >= 32)
+                            chunk_best<32>(acc + c * 32, mw[k], cb, ci);
+                        else
+                            chunk_best<16>(acc + c * 32, mw[k], cb, ci);
+                        if (cb > m) {
+                            m = cb;
+                            am = static_cast<int>(jt) + c * 32 + ci;
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[ab]));
+                    if (++ab == 2) { ab = 0; aph ^= 1; }
+                }
+                if (!ok) break;
+
+                // ---- document end: merge the two warpgroups' (max, argmax)
+                if (half == 1) {
+                    xc->m[par][r] = m;
+                    xc->a[par][r] = am;
+                    if (lane == 0) xc->any[par][quarter] = any;
+                }
+                ptx::mbar_arrive(ptx::smem_u32(&bars->xchg[par]));
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xchg[par]), par ? xph1 : xph0, err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (par) xph1 ^= 1; else xph0 ^= 1;
+                if (!ok) break;
+                if (half == 0) {
+                    const float m1 = xc->m[par][r];
+                    const int a1 = xc->a[par][r];
+                    if (m1 > m || (m1 == m && a1 >= 0 && (am < 0 || a1 < am))) {
+                        m = m1;
+                        am = a1;
+                    }
+                    const bool doc_any = (any | xc->any[par][quarter]) != 0;
+                    const float term = (doc_any && qvalid) ? m : 0.0f;
+                    // per-query sum over the query's rows, in a fixed order
+                    float total = 0.0f;
+                    bool writer = false;
+                    if ((Lq & 31) == 0) {
+                        float s = term;
+#pragma unroll
+                        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                        if (lane == 0) xc->part[par][quarter] = s;
+                        ptx::mbar_arrive(ptx::smem_u32(&bars->qsum[par]));
+                        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qsum[par]), par ? sph1 : sph0, err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (par) sph1 ^= 1; else sph0 ^= 1;
+                        writer = (i == 0);
+                        if (writer) {
+                            const int w0 = r >> 5, nw = static_cast<int>(Lq >> 5);
+                            for (int w = 0; w < nw && w0 + w < 4; ++w) total += xc->part[par][w0 + w];
+                        }
+                    } else if ((32 % Lq) == 0) {
+                        float s = term;
+                        for (int off = static_cast<int>(Lq) >> 1; off > 0; off >>= 1)
+                            s += __shfl_xor_sync(0xffffffffu, s, off);
+                        writer = (i == 0);
+                        total = s;
+                    } else {
+                        xc->part[par][r] = term;
+                        ptx::mbar_arrive(ptx::smem_u32(&bars->qsum[par]));
+                        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qsum[par]), par ? sph1 : sph0, err);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (par) sph1 ^= 1; else sph0 ^= 1;
+                        writer = (i == 0);
+                        if (writer)
+                            for (int64_t k = 0; k < Lq && r + k < kM; ++k) total += xc->part[par][r + k];
+                    }
+                    if (row_ok) {
+                        const int64_t pair = q * p.Nd + d;
+                        if (writer) p.scores[pair] = doc_any ? total : kEmptyDocScore;
+                        if (p.argmax) p.argmax[pair * Lq + i] = (doc_any && qvalid) ? am : -1;
+                    }
+                }
+                par ^= 1;
+                if (!ok) break;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, 2 * kAccCols);
+    }
+}
+
+int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+
+}  // namespace
+
+bool tc_allpairs_eligible(const Problem& P) {
+    return P.layout == kAllPairs && (P.dtype == kF16 || P.dtype == kBF16) && P.dim % 16 == 0 &&
+           P.dim <= 256 && P.Lq >= 1 && P.Lq <= kM && P.Ld >= 1 && P.n_query * P.Lq < (int64_t(1) << 31) &&
+           P.Ld < (int64_t(1) << 31) && P.n_doc < (int64_t(1) << 31);
+}
+
+cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* argmax, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const DeviceInfo& info = device_info(dev);
+
+    Params p{};
+    p.Nq = P.n_query;
+    p.Nd = P.n_doc;
+    p.Lq = P.Lq;
+    p.Ld = P.Ld;
+    p.dim = static_cast<int>(P.dim);
+    p.atoms = (p.dim + kAtomElems - 1) / kAtomElems;
+    const int tmax = p.atoms <= 2 ? 256 : 128;
+    p.tiles_per_doc = ceil_div(P.Ld, tmax);
+    p.T = ((ceil_div(P.Ld, p.tiles_per_doc) + 15) / 16) * 16;
+    p.qpt = static_cast<int>(kM / P.Lq);
+    p.n_rb = ceil_div(P.n_query, p.qpt);
+    p.q_bytes = static_cast<uint32_t>(p.atoms * kM * kAtomBytes);
+    p.d_bytes = static_cast<uint32_t>(p.atoms * p.T * kAtomBytes);
+    const size_t misc = sizeof(Bars) + sizeof(Exchange);
+    const size_t budget = static_cast<size_t>(info.max_smem_optin) - 1024 - misc - 2 * p.q_bytes;
+    p.stages = static_cast<int>(budget / p.d_bytes);
+    if (p.stages > kMaxStages) p.stages = kMaxStages;
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    // documents per work unit: ~24 tiles, but keep at least two units per SM
+    p.dpu = ceil_div(24, p.tiles_per_doc);
+    while (p.dpu > 1 && static_cast<int64_t>(p.n_rb) * ceil_div(P.n_doc, p.dpu) < 2LL * info.sm_count)
+        p.dpu = (p.dpu + 1) / 2;
+    p.n_units = static_cast<int64_t>(p.n_rb) * ceil_div(P.n_doc, p.dpu);
+    p.idesc = ptx::f16_idesc(kM, p.T, P.dtype == kBF16);
+    p.qmask = P.qmask;
+    p.dmask = P.dmask;
+    p.scores = scores;
+    p.argmax = argmax;
+    p.err = device_error_word();
+
+    CUtensorMap tmq, tmd;
+    {
+        const uint64_t dims[2] = {static_cast<uint64_t>(P.dim), static_cast<uint64_t>(P.n_query * P.Lq)};
+        const uint64_t strides[1] = {static_cast<uint64_t>(P.dim) * 2};
+        const uint32_t box[2] = {kAtomElems, kM};
+        if (!encode_tmap_kmajor(&tmq, P.dtype, P.Q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const uint64_t dims[3] = {static_cast<uint64_t>(P.dim), static_cast<uint64_t>(P.Ld),
+                                  static_cast<uint64_t>(P.n_doc)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(P.dim) * 2, static_cast<uint64_t>(P.Ld * P.dim) * 2};
+        const uint32_t box[3] = {kAtomElems, static_cast<uint32_t>(p.T), 1};
+        if (!encode_tmap_kmajor(&tmd, P.dtype, P.D, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+
+    const size_t smem = 1024 + 2 * static_cast<size_t>(p.q_bytes) +
+                        static_cast<size_t>(p.stages) * p.d_bytes + misc;
+    e = cudaFuncSetAttribute(allpairs_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int64_t grid = p.n_units < info.sm_count ? p.n_units : info.sm_count;
+    allpairs_fwd_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmq, tmd, p);
+    return cudaGetLastError();
+}
+
+}  // namespace lik

@@ -1,0 +1,79 @@
+// lik_internal.h -- declarations shared by the translation units of liblik.
+//
+// Not part of the public ABI (include/lik.h is).  Every layout of the
+// operator is described by one Problem: a list of (query, document) pairs
+// in which pair p joins query p / pairs_per_query with
+//   all-pairs:  document p % Nd          (pairs_per_query = Nd)
+//   pairwise:   document p               (pairs_per_query = 1)
+//   kd:         document p  (= b*N + n)  (pairs_per_query = N)
+// and writes scores[p] and argmax[p*Lq .. p*Lq+Lq-1].
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace lik {
+
+enum Layout : int { kAllPairs = 0, kPairwise = 1, kKd = 2 };
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+// Score of a document with no valid token (Late Interaction Kernels README,
+// "Scoring interface").  -1e9 = 15625000 * 2^6 is exact in fp32.
+constexpr float kEmptyDocScore = -1e9f;
+
+struct Problem {
+    int layout;
+    int dtype;
+    const void* Q;            // [n_query, Lq, dim]
+    const void* D;            // [n_doc, Ld, dim]
+    const uint8_t* qmask;     // [n_query, Lq] or nullptr
+    const uint8_t* dmask;     // [n_doc, Ld] or nullptr
+    int64_t n_query;          // Nq | B | B
+    int64_t n_doc;            // Nd | B | B*N
+    int64_t pairs_per_query;  // Nd | 1 | N
+    int64_t n_pairs;          // Nq*Nd | B | B*N
+    int64_t Lq, Ld, dim;
+
+    __host__ __device__ int64_t query_of(int64_t p) const { return p / pairs_per_query; }
+    __host__ __device__ int64_t doc_of(int64_t p) const {
+        return layout == kAllPairs ? p % pairs_per_query : p;
+    }
+};
+
+// Device properties the launchers need, cached per device.
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int major, minor;
+    int max_smem_optin;
+};
+const DeviceInfo& device_info(int device);
+
+// Device address of the library's error word (set by a kernel whose bounded
+// wait expired), for the current device.
+unsigned int* device_error_word();
+
+// Error word codes (bit flags).
+constexpr unsigned int kErrTimeout = 1u;    // a bounded pipeline wait expired
+constexpr unsigned int kErrBadIndex = 2u;   // a saved argmax was >= Ld (skipped)
+
+// ---- launchers (return cudaSuccess or the launch error) ----------------
+
+// Portable FFMA forward for every dtype, layout and size in range.
+cudaError_t launch_fwd_simt(const Problem& P, float* scores, int32_t* argmax,
+                            cudaStream_t stream);
+
+// Tensor-core (tcgen05) all-pairs forward for fp16/bf16: dim % 16 == 0,
+// dim <= 256, 1 <= Lq <= 128, Ld >= 1.
+bool tc_allpairs_eligible(const Problem& P);
+cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* argmax,
+                                   cudaStream_t stream);
+
+// Backward: grad_Q gather and grad_D scatter (grad_D zero-filled first).
+cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,
+                              const int32_t* argmax, float* grad_Q, cudaStream_t stream);
+cudaError_t launch_bwd_grad_d(const Problem& P, const float* grad_out,
+                              const int32_t* argmax, float* grad_D, cudaStream_t stream);
+
+}  // namespace lik

@@ -1,0 +1,118 @@
+"""Run one workload through the CUDA library (C ABI via the binding) and the
+fp64 oracle, and compare them with the rules in ``parity.py``.
+
+Inputs always come from the seeded generators; the oracle never receives a
+value the CUDA library produced.  The backward is checked on the oracle's own
+argmax, fed to both sides.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import parity
+from late_interaction_retrieval_gb300 import binding
+from late_interaction_retrieval_gb300.workloads import Inputs, to_numpy
+
+
+def _np_mask(m):
+    return None if m is None else m.detach().cpu().numpy().astype(np.uint8)
+
+
+class Layout:
+    """Index maps and calls of one layout."""
+
+    def __init__(self, inp: Inputs):
+        self.inp = inp
+        w = inp.workload
+        self.kind = w.layout
+        Q, D = inp.Q, inp.D
+        self.nQ, self.Lq, self.dim = Q.shape
+        if self.kind == "kd":
+            self.B, self.N, self.Ld = D.shape[0], D.shape[1], D.shape[2]
+            self.nD = self.B * self.N
+            self.ppq = self.N
+        else:
+            self.nD, self.Ld = D.shape[0], D.shape[1]
+            self.ppq = self.nD if self.kind == "allpairs" else 1
+        self.n_pairs = self.nQ * self.ppq
+
+    def query_of(self, p):
+        return p // self.ppq
+
+    def doc_of(self, p):
+        return p % self.nD if self.kind == "allpairs" else p
+
+    # ---- oracle ---------------------------------------------------------
+    def oracle_fwd(self):
+        Qn, tag = to_numpy(self.inp.Q)
+        Dn, _ = to_numpy(self.inp.D)
+        qm, dm = _np_mask(self.inp.qmask), _np_mask(self.inp.dmask)
+        return getattr(oracle.get(), f"{self.kind}_fwd")(Qn, Dn, qm, dm, dtype=tag)
+
+    def oracle_bwd(self, grad_out, argmax):
+        Qn, tag = to_numpy(self.inp.Q)
+        Dn, _ = to_numpy(self.inp.D)
+        return getattr(oracle.get(), f"{self.kind}_bwd")(Qn, Dn, grad_out, argmax, dtype=tag)
+
+    # ---- GPU --------------------------------------------------------------
+    def gpu_inputs(self, device="cuda"):
+        i = self.inp
+        mv = lambda t: None if t is None else t.to(device).contiguous()  # noqa: E731
+        return mv(i.Q), mv(i.D), mv(i.qmask), mv(i.dmask)
+
+    def gpu_fwd(self, with_argmax=True, device="cuda"):
+        Q, D, qm, dm = self.gpu_inputs(device)
+        shape = self.inp.workload.score_shape
+        scores = torch.empty(shape, dtype=torch.float32, device=device)
+        am = (torch.full((*shape, self.Lq), -7, dtype=torch.int32, device=device)
+              if with_argmax else None)
+        getattr(binding, f"lik_maxsim_{self.kind}_fwd")(Q, D, qm, dm, scores, am)
+        binding.lik_check_device_error()
+        return scores.cpu().numpy(), None if am is None else am.cpu().numpy()
+
+    def gpu_bwd(self, grad_out, argmax, device="cuda"):
+        Q, D, _, _ = self.gpu_inputs(device)
+        g = torch.as_tensor(np.ascontiguousarray(grad_out), dtype=torch.float32).to(device)
+        am = torch.as_tensor(np.ascontiguousarray(argmax), dtype=torch.int32).to(device)
+        shape = self.inp.workload.score_shape
+        g = g.reshape(shape)
+        am = am.reshape(*shape, self.Lq)
+        gQ = torch.full(Q.shape, float("nan"), dtype=torch.float32, device=device)
+        gD = torch.full(D.shape, float("nan"), dtype=torch.float32, device=device)
+        getattr(binding, f"lik_maxsim_{self.kind}_bwd")(Q, D, g, am, gQ, gD)
+        binding.lik_check_device_error()
+        return gQ.cpu().numpy(), gD.cpu().numpy()
+
+    # ---- comparisons ------------------------------------------------------
+    def check_forward(self):
+        s_o, am_o, gap = self.oracle_fwd()
+        s_g, am_g = self.gpu_fwd()
+        tag = self.inp.workload.dtype
+        err = parity.assert_scores_close(s_g, s_o, tag)
+        Qw = parity.widen(self.inp.Q)
+        Dw = parity.widen(self.inp.D).reshape(self.nD, self.Ld, self.dim)
+        dm = None if self.inp.dmask is None else self.inp.dmask.cpu().numpy().reshape(self.nD, self.Ld)
+        near = parity.assert_argmax_valid(am_g.reshape(self.n_pairs, self.Lq),
+                                          am_o.reshape(self.n_pairs, self.Lq),
+                                          gap.reshape(self.n_pairs, self.Lq), Qw, Dw,
+                                          self.query_of, self.doc_of, dm)
+        # scores without the argmax output must be the same computation
+        s_g2, _ = self.gpu_fwd(with_argmax=False)
+        assert np.array_equal(s_g, s_g2), "scores depend on whether argmax is requested"
+        return dict(score_err=err, near_ties=near, s_oracle=s_o, am_oracle=am_o, am_gpu=am_g)
+
+    def check_backward(self, grad_out=None, am_oracle=None):
+        if am_oracle is None:
+            _, am_oracle, _ = self.oracle_fwd()
+        if grad_out is None:
+            grad_out = self.inp.grad_out.cpu().numpy().astype(np.float64)
+        # both sides get the same fp32 upstream gradient
+        g32 = np.asarray(grad_out, np.float32).astype(np.float64)
+        gQ_o, gD_o = self.oracle_bwd(g32, am_oracle)
+        gQ_g, gD_g = self.gpu_bwd(g32, am_oracle)
+        tag = self.inp.workload.dtype
+        eq = parity.assert_grad_close(gQ_g, gQ_o, tag, "grad_Q")
+        ed = parity.assert_grad_close(gD_g, gD_o, tag, "grad_D")
+        return dict(grad_q_err=eq, grad_d_err=ed)

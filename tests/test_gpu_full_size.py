@@ -1,0 +1,123 @@
+"""CUDA library vs fp64 oracle at the full workload sizes (GPU).
+
+Inputs are drawn on the device by the seeded generators and copied to the
+host for the oracle.  Where the oracle finishes in seconds it runs on every
+pair (in-batch, per-query candidates, reranking); on the large all-pairs
+inference workload it scores a seeded sample of (query, document) pairs one
+by one.  Gradients are checked on sampled query and document rows by
+running the oracle backward on the sub-problem that owns them, with the
+oracle's own argmax fed to the GPU backward.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness
+import oracle
+import parity
+from late_interaction_retrieval_gb300 import binding
+from late_interaction_retrieval_gb300.workloads import ce_grad_rows, generate, to_numpy
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_scores_argmax(h, inp):
+    Q, D = inp.Q.contiguous(), inp.D.contiguous()
+    shape = inp.workload.score_shape
+    scores = torch.empty(shape, dtype=torch.float32, device=Q.device)
+    am = torch.empty((*shape, h.Lq), dtype=torch.int32, device=Q.device)
+    getattr(binding, f"lik_maxsim_{h.kind}_fwd")(Q, D, inp.qmask, inp.dmask, scores, am)
+    binding.lik_check_device_error()
+    return scores, am
+
+
+def _check_full_forward(name):
+    inp = generate(name, device="cuda")
+    h = gpu_harness.Layout(inp)
+    s_g, am_g = _gpu_scores_argmax(h, inp)
+    s_o, am_o, gap = h.oracle_fwd()
+    tag = inp.workload.dtype
+    parity.assert_scores_close(s_g.cpu().numpy(), s_o, tag)
+    Qw = parity.widen(inp.Q)
+    Dw = parity.widen(inp.D).reshape(h.nD, h.Ld, h.dim)
+    dm = inp.dmask.cpu().numpy().reshape(h.nD, h.Ld)
+    parity.assert_argmax_valid(am_g.cpu().numpy().reshape(h.n_pairs, h.Lq),
+                               am_o.reshape(h.n_pairs, h.Lq), gap.reshape(h.n_pairs, h.Lq),
+                               Qw, Dw, h.query_of, h.doc_of, dm)
+    return inp, h, s_o, am_o
+
+
+def test_inbatch_b128_bf16_full():
+    inp, h, s_o, am_o = _check_full_forward("inbatch_b128_bf16")
+    g = ce_grad_rows(torch.from_numpy(s_o), inp.ce_target.cpu()).numpy()
+    g32 = g.astype(np.float32)
+    gQ_g, gD_g = h.gpu_bwd(g32, am_o)
+    Qn, tag = to_numpy(inp.Q)
+    Dn, _ = to_numpy(inp.D)
+    orc = oracle.get()
+    rng = np.random.default_rng(0)
+    for q in rng.choice(h.nQ, 6, replace=False):
+        gQ_o, _ = orc.allpairs_bwd(Qn[q:q + 1], Dn, g32[q:q + 1].astype(np.float64),
+                                   am_o[q:q + 1], dtype=tag)
+        parity.assert_grad_close(gQ_g[q], gQ_o[0], "bf16", f"grad_Q[{q}]")
+    for d in rng.choice(h.nD, 6, replace=False):
+        _, gD_o = orc.allpairs_bwd(Qn, Dn[d:d + 1], g32[:, d:d + 1].astype(np.float64),
+                                   am_o[:, d:d + 1], dtype=tag)
+        parity.assert_grad_close(gD_g[d], gD_o[0], "bf16", f"grad_D[{d}]")
+
+
+def test_kd_b256_n17_bf16_full():
+    inp, h, s_o, am_o = _check_full_forward("kd_b256_n17_bf16")
+    # the planted positive (candidate 0) scores highest for most queries
+    assert np.mean(np.argmax(s_o, axis=1) == 0) > 0.9
+    g = ce_grad_rows(torch.from_numpy(s_o), inp.ce_target.cpu()).numpy()
+    g32 = g.astype(np.float32)
+    gQ_g, gD_g = h.gpu_bwd(g32, am_o)
+    Qn, tag = to_numpy(inp.Q)
+    Dn, _ = to_numpy(inp.D)
+    orc = oracle.get()
+    rng = np.random.default_rng(1)
+    for b in rng.choice(h.nQ, 8, replace=False):
+        gQ_o, gD_o = orc.kd_bwd(Qn[b:b + 1], Dn[b:b + 1], g32[b:b + 1].astype(np.float64),
+                                am_o[b:b + 1], dtype=tag)
+        parity.assert_grad_close(gQ_g[b], gQ_o[0], "bf16", f"grad_Q[{b}]")
+        parity.assert_grad_close(gD_g[b], gD_o[0], "bf16", f"grad_D[{b}]")
+    # rows no argmax points at are exactly zero
+    hit = np.zeros((h.nD, h.Ld), bool)
+    pairs, toks = np.nonzero(am_o.reshape(h.n_pairs, h.Lq) >= 0)
+    hit[pairs, am_o.reshape(h.n_pairs, h.Lq)[pairs, toks]] = True
+    row_max = np.abs(gD_g.reshape(h.nD, h.Ld, h.dim)).max(axis=2)
+    assert not np.any(row_max[~hit])
+
+
+def test_rerank_b512_ld8192_f16_full():
+    _check_full_forward("rerank_b512_ld8192_f16")
+
+
+def test_allpairs_q128_d4096_bf16_sampled():
+    inp = generate("allpairs_q128_d4096_bf16", device="cuda")
+    h = gpu_harness.Layout(inp)
+    s_g, am_g = _gpu_scores_argmax(h, inp)
+    s_g, am_g = s_g.cpu().numpy(), am_g.cpu().numpy()
+    rng = np.random.default_rng(2)
+    qs = rng.integers(0, h.nQ, 48)
+    ds = rng.integers(0, h.nD, 48)
+    # include short documents (the 10% with random lengths)
+    short = torch.nonzero(~inp.dmask[:, -1]).flatten().cpu().numpy()
+    ds[:12] = rng.choice(short, 12, replace=False)
+    orc = oracle.get()
+    ref, got = [], []
+    for q, d in zip(qs, ds):
+        qw = parity.widen(inp.Q[q])
+        dw = parity.widen(inp.D[d])
+        dm = inp.dmask[d].cpu().numpy()
+        qm = inp.qmask[q].cpu().numpy()
+        s, am, gap = orc.pair(qw, dw, qm, dm)
+        ref.append(s)
+        got.append(s_g[q, d])
+        sure = gap > parity.GAP_EXACT
+        assert np.array_equal(am_g[q, d][sure], am[sure]), (q, d)
+        for i in np.flatnonzero(~sure & (am_g[q, d] != am)):
+            a = am_g[q, d, i]
+            assert dm[a] and qw[i] @ dw[a] >= qw[i] @ dw[am[i]] - parity.NEAR_TIE
+    parity.assert_scores_close(np.array(got), np.array(ref), "bf16")
