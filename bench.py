@@ -1,0 +1,508 @@
+"""Benchmark of the MaxSim hot path on GB300.
+
+Default workload: the in-batch contrastive all-pairs forward + backward, bf16
+in / fp32 scores, Q[128,32,128] x D[128,1030,128], document lengths
+U[700,1030], grad_out from row-wise cross-entropy with the diagonal as
+target.  One step = liblik forward (scores + saved argmax) and backward
+(grad_Q, grad_D) through the C ABI, inputs resident in HBM.  The headline
+metric counts 2*Nq*Nd*Lq*Ld*dim FLOPs (padded Ld) per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle, as it stands
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload (weak scaling, no collective on the data path); timings are
+max-reduced over ranks and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from late_interaction_retrieval_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MaxSim fwd+bwd TFLOP/s (% dense bf16 peak); pairwise GB/s (% HBM peak)"
+L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = {
+    "allpairs_fwd_tc_kernel": "late_interaction_retrieval_gb300/csrc/fwd_tc_allpairs.cu",
+    "stream_fwd_tc_kernel": "late_interaction_retrieval_gb300/csrc/fwd_tc_stream.cu",
+}
+
+
+# ------------------------------------------------------------ utilities --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the capture (else None)."""
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    with open(PROFILE_TRAFFIC) as f:
+        table = json.load(f)
+    ent = table.get(kernel, {}).get(workload)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if ent.get("source_sha256") != sha:
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: torch.device):
+        self.gpu = self._smi_id(device)
+        self.proc = None
+        self.path = None
+
+    @staticmethod
+    def _smi_id(device) -> str:
+        """nvidia-smi id of a torch device (its UUID; CUDA_VISIBLE_DEVICES may renumber)."""
+        try:
+            u = str(torch.cuda.get_device_properties(device).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = device.index or 0
+            if vis:
+                return vis.split(",")[idx].strip()
+            return str(idx)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload --
+
+class Step:
+    """Device buffers and the liblik calls of one step of a workload."""
+
+    def __init__(self, name: str, device: torch.device):
+        from late_interaction_retrieval_gb300 import binding
+        self.binding = binding
+        self.w = W.WORKLOADS[name]
+        self.inp = W.generate(name, device=device)
+        self.device = device
+        w, i = self.w, self.inp
+        self.layout = w.layout
+        self.scores = torch.empty(w.score_shape, dtype=torch.float32, device=device)
+        self.argmax = (torch.empty((*w.score_shape, w.lq), dtype=torch.int32, device=device)
+                       if w.backward else None)
+        self.gQ = torch.empty(i.Q.shape, dtype=torch.float32, device=device) if w.backward else None
+        self.gD = torch.empty(i.D.shape, dtype=torch.float32, device=device) if w.backward else None
+        self.fwd()
+        torch.cuda.synchronize()
+        if w.backward:
+            if i.grad_out is not None:
+                self.g = i.grad_out.to(device).float().contiguous()
+            else:  # cross-entropy head of the workload: computed once, outside the timed steps
+                self.g = W.ce_grad_rows(self.scores, i.ce_target).float().contiguous()
+        binding.lik_check_device_error()
+
+    def fwd(self, Q=None, D=None, qm=None, dm=None):
+        i = self.inp
+        Q = i.Q if Q is None else Q
+        D = i.D if D is None else D
+        qm = i.qmask if qm is None else qm
+        dm = i.dmask if dm is None else dm
+        getattr(self.binding, f"lik_maxsim_{self.layout}_fwd")(Q, D, qm, dm, self.scores, self.argmax)
+
+    def bwd(self, Q=None, D=None, g=None):
+        i = self.inp
+        getattr(self.binding, f"lik_maxsim_{self.layout}_bwd")(
+            i.Q if Q is None else Q, i.D if D is None else D, self.g if g is None else g,
+            self.argmax, self.gQ, self.gD)
+
+    # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours)
+    @property
+    def launches_per_step(self) -> int:
+        return 1 + (2 if self.w.backward else 0)
+
+    def valid_flops(self) -> int:
+        i, w = self.inp, self.w
+        qv = i.qmask.sum(dim=1).double()  # [nq]
+        dv = i.dmask.reshape(-1, w.ld).sum(dim=1).double()  # [n_doc]
+        if w.layout == "allpairs":
+            tot = float(qv.sum() * dv.sum())
+        elif w.layout == "pairwise":
+            tot = float((qv * dv).sum())
+        else:
+            tot = float((qv[:, None] * dv.view(w.nq, w.nd)).sum())
+        return int(2 * w.dim * tot)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes a forward must move at least: valid D rows, Q, masks, scores."""
+        i, w = self.inp, self.w
+        el = i.Q.element_size()
+        dv = int(i.dmask.sum())
+        qbytes = i.Q.numel() * el
+        return dv * w.dim * el + i.dmask.numel() + qbytes + i.qmask.numel() + self.scores.numel() * 4
+
+
+# ---------------------------------------------------------------- our arm --
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    name = args.workload
+    st = Step(name, device)
+    w = st.w
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def one_step():
+        st.fwd()
+        if w.backward:
+            st.bwd()
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+    st.binding.lik_check_device_error()
+
+    # ---- device-timed steps, inputs resident in HBM, L2 flushed in between
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(device).start()
+    time.sleep(0.15)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        e0, e1, e2 = ev[k]
+        e0.record(stream)
+        st.fwd()
+        e1.record(stream)
+        if w.backward:
+            st.bwd()
+        e2.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    # keep the same load until the clock sampler has seen >= 1 s of it
+    while time.perf_counter() - t_wall0 < 1.0:
+        for _ in range(20):
+            flush.zero_()
+            one_step()
+        torch.cuda.synchronize()
+    clocks = sampler.stop()
+    st.binding.lik_check_device_error()
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    e2e = run_e2e(st, args, stream, world)
+
+    if rank == 0:
+        peaks = measured_peaks()
+        ms_per_step = total_ms / args.steps
+        fwd_avg_ms = statistics.mean(fwd_ms)
+        counted = w.counted_flops
+        fwd_only_pairwise = (w.layout == "pairwise" and not w.backward)
+        if fwd_only_pairwise:
+            units = st.algorithmic_bytes()
+            value = world * args.steps * units / (total_ms * 1e-3) / 1e9
+            unit = "GB/s"
+            roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+            kernel = "stream_fwd_tc_kernel"
+        else:
+            value = world * args.steps * counted / (total_ms * 1e-3) / 1e12
+            unit = "TFLOP/s"
+            kernel = "allpairs_fwd_tc_kernel" if w.layout == "allpairs" else "stream_fwd_tc_kernel"
+            if w.layout == "kd":
+                units = st.algorithmic_bytes()
+                roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9,
+                        "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+            else:
+                roof = {"bound": "tensor", "achieved": counted / (fwd_avg_ms * 1e-3) / 1e12,
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = kernel_traffic(kernel, name)
+        roof["kernel"] = kernel
+        roof["peak_source"] = f"{peaks['source']} (burst; kernel timed alone within a short step)"
+        roof["kernel_ms"] = fwd_avg_ms
+        cpu = cpu_baseline(name, unit) if not args.no_cpu_baseline else None
+        line = {
+            "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic (seeded, L2-normalised Gaussian tokens)",
+            "config": {
+                "workload": name, "layout": w.layout,
+                "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
+                "counted_flops_per_step": counted, "valid_token_flops_per_step": st.valid_flops(),
+                "algorithmic_fwd_bytes": st.algorithmic_bytes(),
+                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                "fwd_ms": fwd_avg_ms, "wall_s": t_wall,
+            },
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": st.launches_per_step * args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(st: Step, args, stream, world):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads back scores and gradients."""
+    i, w = st.inp, st.w
+    host = {k: v.cpu().pin_memory() for k, v in
+            (("Q", i.Q), ("D", i.D), ("qm", i.qmask), ("dm", i.dmask))}
+    if w.backward:
+        host["g"] = st.g.cpu().pin_memory()
+    dev = {k: torch.empty_like(v, device=st.device) for k, v in host.items()}
+    outs = [st.scores] + ([st.gQ, st.gD] if w.backward else [])
+    back = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        st.fwd(dev["Q"], dev["D"], dev["qm"], dev["dm"])
+        if w.backward:
+            st.bwd(dev["Q"], dev["D"], dev["g"])
+        for o, b in zip(outs, back):
+            b.copy_(o, non_blocking=True)
+
+    n = max(3, min(args.steps, 20))
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=st.device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if w.layout == "pairwise" and not w.backward:
+        val, unit = world * n * st.algorithmic_bytes() / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        val, unit = world * n * w.counted_flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    return {"value": val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "ms_per_step": ms / n}
+
+
+# ------------------------------------------------------------- oracle arm --
+
+def oracle_sample(name: str, budget_s: float, max_steps: int | None = None):
+    """Run the fp64 oracle on query subsets of the workload until `budget_s`
+    seconds (or `max_steps` subsets) have passed.  Returns (list of per-subset
+    (seconds, counted_flops, bytes)), threads, description."""
+    import numpy as np
+
+    import oracle
+    orc = oracle.get()
+    w = W.WORKLOADS[name]
+    inp = W.generate(name, device="cpu") if w.layout != "kd" else None
+    if inp is None:  # the kd workload is large to draw on the CPU: use the same recipe on fewer queries
+        inp = W.generate(name, device="cuda" if torch.cuda.is_available() else "cpu")
+    Qn, tag = W.to_numpy(inp.Q)
+    Dn, _ = W.to_numpy(inp.D)
+    qm = inp.qmask.cpu().numpy()
+    dm = inp.dmask.cpu().numpy()
+    per_q = w.counted_flops // w.nq
+    sub = 1
+    results = []
+    t_start = time.perf_counter()
+    q0 = 0
+    while True:
+        qs = slice(q0 % w.nq, q0 % w.nq + sub)
+        t0 = time.perf_counter()
+        if w.layout == "allpairs":
+            s, am, _ = orc.allpairs_fwd(Qn[qs], Dn, qm[qs], dm, dtype=tag)
+            if w.backward:
+                g = np.random.default_rng(0).standard_normal(s.shape)
+                orc.allpairs_bwd(Qn[qs], Dn, g, am, dtype=tag)
+        elif w.layout == "pairwise":
+            s, am, _ = orc.pairwise_fwd(Qn[qs], Dn[qs], qm[qs], dm[qs], dtype=tag)
+        else:
+            s, am, _ = orc.kd_fwd(Qn[qs], Dn[qs], qm[qs], dm[qs], dtype=tag)
+            if w.backward:
+                g = np.random.default_rng(0).standard_normal(s.shape)
+                orc.kd_bwd(Qn[qs], Dn[qs], g, am, dtype=tag)
+        dt = time.perf_counter() - t0
+        results.append((dt, per_q * sub))
+        q0 += sub
+        if max_steps is not None and len(results) >= max_steps:
+            break
+        if max_steps is None and time.perf_counter() - t_start >= budget_s:
+            break
+    desc = (f"{name}: {sum(r[1] for r in results) // per_q} single-query passes (query q against "
+            f"all of its documents, cycling over the {w.nq} queries), "
+            f"{'fwd+bwd' if w.backward else 'fwd'}, fp64")
+    return results, orc.num_threads(), desc
+
+
+def cpu_baseline(name: str, unit: str):
+    results, cores, desc = oracle_sample(name, budget_s=12.0)
+    secs = sum(r[0] for r in results)
+    flops = sum(r[1] for r in results)
+    w = W.WORKLOADS[name]
+    if unit == "GB/s":
+        frac = flops / w.counted_flops
+        val = frac * fwd_bytes(name) / secs / 1e9
+    else:
+        val = flops / secs / 1e12
+    return {"value": val, "unit": unit, "cores": cores, "kind": "oracle",
+            "sample": desc + f", {secs:.1f} s"}
+
+
+def fwd_bytes(name: str) -> int:
+    """Algorithmic forward bytes of the full workload (CPU-side recount)."""
+    w = W.WORKLOADS[name]
+    inp = W.generate(name, device="cuda" if torch.cuda.is_available() else "cpu")
+    el = inp.Q.element_size()
+    return (int(inp.dmask.sum()) * w.dim * el + inp.dmask.numel() + inp.Q.numel() * el
+            + inp.qmask.numel() + math.prod(w.score_shape) * 4)
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    name = args.workload
+    w = W.WORKLOADS[name]
+    results, cores, desc = oracle_sample(name, budget_s=0, max_steps=args.warmup + args.steps)
+    timed = results[args.warmup:]
+    secs = sum(r[0] for r in timed)
+    flops = sum(r[1] for r in timed)
+    if w.layout == "pairwise" and not w.backward:
+        unit = "GB/s"
+        value = flops / w.counted_flops * fwd_bytes(name) / secs / 1e9
+    else:
+        unit = "TFLOP/s"
+        value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / max(len(timed), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded, L2-normalised Gaussian tokens)",
+        "config": {"workload": name, "layout": w.layout, "Q": list(w.q_shape), "D": list(w.d_shape),
+                   "passes": "fwd+bwd" if w.backward else "fwd",
+                   "step": "one query of the workload against all its documents"},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="inbatch_b128_bf16", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
