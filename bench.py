@@ -52,6 +52,21 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(x: float, device) -> float:
+    """Max of a per-rank float over the default process group (identity at N=1)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, steps: int, units_per_step: float, max_ms: float, scale: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time (weak scaling)."""
+    return world * steps * units_per_step / (max_ms * 1e-3) / scale
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -269,11 +284,7 @@ def run_ours(args):
     st.binding.lik_check_device_error()
     step_ms = [a.elapsed_time(c) for a, _, c in ev]
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), device)
 
     # ---- end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(st, args, stream, world)
@@ -286,13 +297,13 @@ def run_ours(args):
         fwd_only_pairwise = (w.layout == "pairwise" and not w.backward)
         if fwd_only_pairwise:
             units = st.algorithmic_bytes()
-            value = world * args.steps * units / (total_ms * 1e-3) / 1e9
+            value = whole_job_rate(world, args.steps, units, total_ms, 1e9)
             unit = "GB/s"
             roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9,
                     "peak": peaks["hbm_gbs"], "unit": "GB/s"}
             kernel = "stream_fwd_tc_kernel"
         else:
-            value = world * args.steps * counted / (total_ms * 1e-3) / 1e12
+            value = whole_job_rate(world, args.steps, counted, total_ms, 1e12)
             unit = "TFLOP/s"
             kernel = "allpairs_fwd_tc_kernel" if w.layout == "allpairs" else "stream_fwd_tc_kernel"
             if w.layout == "kd":
@@ -369,15 +380,11 @@ def run_e2e(st: Step, args, stream, world):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=st.device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), st.device)
     if w.layout == "pairwise" and not w.backward:
-        val, unit = world * n * st.algorithmic_bytes() / (ms * 1e-3) / 1e9, "GB/s"
+        val, unit = whole_job_rate(world, n, st.algorithmic_bytes(), ms, 1e9), "GB/s"
     else:
-        val, unit = world * n * w.counted_flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+        val, unit = whole_job_rate(world, n, w.counted_flops, ms, 1e12), "TFLOP/s"
     return {"value": val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "ms_per_step": ms / n}
 
