@@ -37,8 +37,9 @@
  *
  * Memory, ownership, streams:
  *   - Every pointer is a device pointer (cudaMalloc or managed memory) of
- *     the current device, row-major and contiguous.  Q and D must be 16-byte
- *     aligned.  Host pointers are rejected with LIK_ERR_INVALID_ARG.
+ *     the current device, row-major and contiguous.  Q, D, grad_Q and grad_D
+ *     must be 16-byte aligned; scores, argmax and grad_out 4-byte aligned.
+ *     Host pointers are rejected with LIK_ERR_INVALID_ARG.
  *   - The caller allocates every buffer, outputs included.  The library
  *     allocates no device memory and keeps no per-call state.
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream).

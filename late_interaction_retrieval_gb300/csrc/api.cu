@@ -162,6 +162,12 @@ lik_status check_alignment(const void* Q, const void* D) {
     return LIK_OK;
 }
 
+lik_status check_aligned(const void* p, uintptr_t bytes, const char* name) {
+    if (reinterpret_cast<uintptr_t>(p) & (bytes - 1))
+        return fail(LIK_ERR_INVALID_ARG, "%s must be %d-byte aligned", name, static_cast<int>(bytes));
+    return LIK_OK;
+}
+
 Problem make_problem(int layout, lik_dtype dtype, const void* Q, const void* D,
                      const bool* qmask, const bool* dmask, int64_t n_query, int64_t n_doc,
                      int64_t ppq, int64_t n_pairs, int64_t Lq, int64_t Ld, int64_t dim) {
@@ -198,6 +204,8 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
     };
     if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
     if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
+    if ((st = check_aligned(scores, 4, "scores")) != LIK_OK) return st;
+    if ((st = check_aligned(argmax, 4, "argmax")) != LIK_OK) return st;
     const bool tc = tc_allpairs_eligible(P);
     cudaError_t e = tc ? launch_fwd_tc_allpairs(P, scores, argmax, stream)
                        : launch_fwd_simt(P, scores, argmax, stream);
@@ -224,6 +232,10 @@ lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argma
     };
     if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
     if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
+    if ((st = check_aligned(grad_out, 4, "grad_out")) != LIK_OK) return st;
+    if ((st = check_aligned(argmax, 4, "argmax")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_Q, 16, "grad_Q")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_D, 16, "grad_D")) != LIK_OK) return st;
     cudaError_t e;
     if (grad_Q && (e = launch_bwd_grad_q(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess)
         return cuda_fail(e, "grad_Q launch");

@@ -12,7 +12,9 @@
 // argmax -1 (masked query token, empty document) contributes nothing.  The
 // backward allocates nothing: it writes the two input gradients only (colpali
 // PR "Add support for late-interaction-kernels (LIK)", Results: the fused
-// backward allocates only the input gradients).
+// backward allocates only the input gradients).  Every saved argmax is
+// checked: an index >= Ld is skipped (never dereferenced) and flagged in the
+// library's error word.
 #include "dtype_load.cuh"
 #include "lik_internal.h"
 
@@ -22,9 +24,148 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 
-// One warp per (query, token) row of grad_Q; lanes stride over dim.  The
-// pairs of a query are visited in ascending order, so the fp32 sum order is
-// fixed.
+// ------------------------------------------------------------- grad_Q --
+//
+// Vector path (dim % 8 == 0, dim <= 256): one CTA per (query, group of 32
+// query tokens), 2 x 256 threads.  Eight threads own one token row, each a
+// set of 8-element vectors (16 B of fp16/bf16); the two 256-thread halves
+// take alternate pairs of the query.  The pairs are visited in chunks whose
+// argmax slice and upstream gradients (both contiguous in memory) are staged
+// in shared memory; every thread then gathers its document rows with
+// independent 16-byte loads, four pairs at a time.  The halves' partial sums
+// are added in a fixed order at the end, so the result is deterministic.
+
+constexpr int kRowsPerCta = 32;
+constexpr int kThreadsPerRow = 8;
+constexpr int kPairGroups = 2;
+constexpr int kVecThreads = kRowsPerCta * kThreadsPerRow * kPairGroups;  // 512
+constexpr int kVec = 8;                                                  // elements per vector
+constexpr int kPairChunk = 64;
+
+struct Vec8 {
+    float v[kVec];
+};
+
+__device__ __forceinline__ Vec8 load_vec8(const float* p) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4);
+    return {{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
+}
+__device__ __forceinline__ Vec8 load_vec8(const __half* p) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const __half2* h = reinterpret_cast<const __half2*>(&r);
+    Vec8 o;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float2 f = __half22float2(h[t]);
+        o.v[2 * t] = f.x;
+        o.v[2 * t + 1] = f.y;
+    }
+    return o;
+}
+__device__ __forceinline__ Vec8 load_vec8(const __nv_bfloat16* p) {
+    const uint4 r = *reinterpret_cast<const uint4*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+    Vec8 o;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const float2 f = __bfloat1622float2(h[t]);
+        o.v[2 * t] = f.x;
+        o.v[2 * t + 1] = f.y;
+    }
+    return o;
+}
+
+// VECS vectors of 8 elements per thread: dim <= VECS * 64.
+template <typename T, int VECS>
+__global__ void __launch_bounds__(kVecThreads)
+grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                  float* __restrict__ gQ, unsigned int* err) {
+    __shared__ int s_am[kPairChunk][kRowsPerCta];
+    __shared__ float s_g[kPairChunk];
+    __shared__ float s_part[kRowsPerCta][VECS * kThreadsPerRow * kVec];
+    const T* D = static_cast<const T*>(P.D);
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t q = blockIdx.x / groups;
+    const int64_t i0 = (blockIdx.x - q * groups) * kRowsPerCta;
+    const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group 0 / 1
+    const int tl = threadIdx.x % (kRowsPerCta * kThreadsPerRow);
+    const int r = tl / kThreadsPerRow, sub = tl % kThreadsPerRow;
+    const int rows_here = static_cast<int>(P.Lq - i0 < kRowsPerCta ? P.Lq - i0 : kRowsPerCta);
+
+    float acc[VECS][kVec];
+#pragma unroll
+    for (int m = 0; m < VECS; ++m)
+#pragma unroll
+        for (int t = 0; t < kVec; ++t) acc[m][t] = 0.f;
+
+    const int64_t p0 = q * P.pairs_per_query;
+    bool bad = false;
+    for (int64_t c0 = 0; c0 < P.pairs_per_query; c0 += kPairChunk) {
+        const int nc = static_cast<int>(P.pairs_per_query - c0 < kPairChunk ? P.pairs_per_query - c0 : kPairChunk);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nc * kRowsPerCta; e += kVecThreads) {
+            const int t = e / kRowsPerCta, rr = e % kRowsPerCta;
+            s_am[t][rr] = rr < rows_here ? am[(p0 + c0 + t) * P.Lq + i0 + rr] : -1;
+        }
+        for (int t = threadIdx.x; t < nc; t += kVecThreads) s_g[t] = g[p0 + c0 + t];
+        __syncthreads();
+        if (r >= rows_here) continue;
+        // this half takes pairs t = pg, pg + 2, pg + 4, ... of the chunk
+        for (int t = pg; t < nc; t += 4 * kPairGroups) {
+            const T* rows[4];
+            float gv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int tt = t + u * kPairGroups;
+                int a = tt < nc ? s_am[tt][r] : -1;
+                if (a >= P.Ld) {
+                    bad = true;
+                    a = -1;
+                }
+                gv[u] = a >= 0 ? s_g[tt] : 0.f;
+                rows[u] = a >= 0 ? D + (P.doc_of(p0 + c0 + tt) * P.Ld + a) * P.dim : nullptr;
+            }
+#pragma unroll
+            for (int m = 0; m < VECS; ++m) {
+                const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
+                if (k >= P.dim) break;
+                Vec8 x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (rows[u]) x[u] = load_vec8(rows[u] + k);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (rows[u])
+#pragma unroll
+                        for (int e = 0; e < kVec; ++e) acc[m][e] = fmaf(gv[u], x[u].v[e], acc[m][e]);
+            }
+        }
+    }
+    if (bad) atomicOr(err, kErrBadIndex);
+    __syncthreads();
+    if (pg == 1 && r < rows_here) {
+#pragma unroll
+        for (int m = 0; m < VECS; ++m)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) s_part[r][(m * kThreadsPerRow + sub) * kVec + e] = acc[m][e];
+    }
+    __syncthreads();
+    if (pg == 1 || r >= rows_here) return;
+    float* out = gQ + (q * P.Lq + i0 + r) * P.dim;
+#pragma unroll
+    for (int m = 0; m < VECS; ++m) {
+        const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
+        if (k >= P.dim) break;
+        float o[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) o[e] = acc[m][e] + s_part[r][k + e];
+        *reinterpret_cast<float4*>(out + k) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(out + k + 4) = make_float4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// Any-dim path: one warp per (query, token) row; lanes stride over dim.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 grad_q_gather_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
@@ -62,8 +203,87 @@ grad_q_gather_kernel(Problem P, const float* __restrict__ g, const int32_t* __re
     }
 }
 
-// One warp per (pair, token) hit; adds g * Q[q,i,:] into grad_D[d, a, :]
-// with fp32 atomics.  grad_D is zero-filled on the stream first.
+// ------------------------------------------------------------- grad_D --
+//
+// grad_D is zero-filled on the stream, then every (pair, token) hit adds
+// g * Q[q,i,:] into grad_D[d, a, :].  Vector path (dim % 4 == 0): each lane
+// adds 4 consecutive fp32 with one 16-byte reduction (red.global.add.v4.f32),
+// a warp covers 128 dims of one hit, and each warp keeps two hits in flight.
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void load4(const float* p, float (&o)[4]) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    o[0] = v.x;
+    o[1] = v.y;
+    o[2] = v.z;
+    o[3] = v.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&o)[4]) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
+    const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+    o[0] = a.x;
+    o[1] = a.y;
+    o[2] = b.x;
+    o[3] = b.y;
+}
+__device__ __forceinline__ void load4(const __half* p, float (&o)[4]) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p);
+    const __half2* h = reinterpret_cast<const __half2*>(&r);
+    const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
+    o[0] = a.x;
+    o[1] = a.y;
+    o[2] = b.x;
+    o[3] = b.y;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+grad_d_scatter_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                          float* __restrict__ gD, unsigned int* err) {
+    const T* Q = static_cast<const T*>(P.Q);
+    const int lane = threadIdx.x & 31;
+    const int64_t hits = P.n_pairs * P.Lq;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps * 2;
+    for (int64_t h0 = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * 2; h0 < hits;
+         h0 += stride) {
+        int32_t a[2];
+        float gv[2];
+        const T* qrow[2];
+        float* out[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t h = h0 + u;
+            a[u] = h < hits ? am[h] : -1;
+            if (a[u] >= P.Ld) {
+                if (lane == 0) atomicOr(err, kErrBadIndex);
+                a[u] = -1;
+            }
+            const int64_t p = h / P.Lq, i = h - p * P.Lq;
+            gv[u] = a[u] >= 0 ? g[p] : 0.f;
+            qrow[u] = Q + (P.query_of(p) * P.Lq + i) * P.dim;
+            out[u] = gD + (P.doc_of(p) * P.Ld + (a[u] >= 0 ? a[u] : 0)) * P.dim;
+        }
+        for (int64_t k = lane * 4; k < P.dim; k += 128) {
+            float x[2][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (a[u] >= 0) load4(qrow[u] + k, x[u]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (a[u] >= 0)
+                    red_add_v4(out[u] + k, gv[u] * x[u][0], gv[u] * x[u][1], gv[u] * x[u][2],
+                               gv[u] * x[u][3]);
+        }
+    }
+}
+
+// Any-dim path: one warp per hit, scalar fp32 atomics.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 grad_d_scatter_atomic_kernel(Problem P, const float* __restrict__ g,
@@ -88,30 +308,54 @@ grad_d_scatter_atomic_kernel(Problem P, const float* __restrict__ g,
     }
 }
 
-unsigned grid_for(int64_t warps_of_work) {
+unsigned grid_for(int64_t warps_of_work, int per_sm) {
     int dev = 0;
     cudaGetDevice(&dev);
-    const int64_t cap = static_cast<int64_t>(device_info(dev).sm_count) * 16;
+    const int64_t cap = static_cast<int64_t>(device_info(dev).sm_count) * per_sm;
     int64_t blocks = (warps_of_work + kWarps - 1) / kWarps;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     return static_cast<unsigned>(blocks);
 }
 
+template <typename T>
+cudaError_t grad_q_typed(const Problem& P, const float* g, const int32_t* am, float* gQ,
+                         cudaStream_t stream, unsigned int* err) {
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t blocks = P.n_query * groups;
+    if (P.dim % kVec == 0 && P.dim <= 256 && blocks < (int64_t(1) << 31)) {
+        if (P.dim <= 128)
+            grad_q_vec_kernel<T, 2><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+        else
+            grad_q_vec_kernel<T, 4><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+        return cudaGetLastError();
+    }
+    grad_q_gather_kernel<T><<<grid_for(P.n_query * P.Lq, 16), kThreads, 0, stream>>>(P, g, am, gQ, err);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t grad_d_typed(const Problem& P, const float* g, const int32_t* am, float* gD,
+                         cudaStream_t stream, unsigned int* err) {
+    const int64_t hits = P.n_pairs * P.Lq;
+    if (P.dim % 4 == 0)
+        grad_d_scatter_vec_kernel<T><<<grid_for((hits + 1) / 2, 16), kThreads, 0, stream>>>(P, g, am, gD, err);
+    else
+        grad_d_scatter_atomic_kernel<T><<<grid_for(hits, 16), kThreads, 0, stream>>>(P, g, am, gD, err);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_grad_q(const Problem& P, const float* g, const int32_t* am, float* gQ,
                               cudaStream_t stream) {
-    const int64_t rows = P.n_query * P.Lq;
-    if (rows == 0) return cudaSuccess;
-    const unsigned blocks = grid_for(rows);
+    if (P.n_query * P.Lq == 0) return cudaSuccess;
     unsigned int* err = device_error_word();
     switch (P.dtype) {
-    case kF32: grad_q_gather_kernel<float><<<blocks, kThreads, 0, stream>>>(P, g, am, gQ, err); break;
-    case kF16: grad_q_gather_kernel<__half><<<blocks, kThreads, 0, stream>>>(P, g, am, gQ, err); break;
-    default: grad_q_gather_kernel<__nv_bfloat16><<<blocks, kThreads, 0, stream>>>(P, g, am, gQ, err);
+    case kF32: return grad_q_typed<float>(P, g, am, gQ, stream, err);
+    case kF16: return grad_q_typed<__half>(P, g, am, gQ, stream, err);
+    default: return grad_q_typed<__nv_bfloat16>(P, g, am, gQ, stream, err);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_grad_d(const Problem& P, const float* g, const int32_t* am, float* gD,
@@ -120,16 +364,13 @@ cudaError_t launch_bwd_grad_d(const Problem& P, const float* g, const int32_t* a
     if (elems == 0) return cudaSuccess;
     const cudaError_t e = cudaMemsetAsync(gD, 0, sizeof(float) * elems, stream);
     if (e != cudaSuccess) return e;
-    const int64_t hits = P.n_pairs * P.Lq;
-    if (hits == 0) return cudaSuccess;
-    const unsigned blocks = grid_for(hits);
+    if (P.n_pairs * P.Lq == 0) return cudaSuccess;
     unsigned int* err = device_error_word();
     switch (P.dtype) {
-    case kF32: grad_d_scatter_atomic_kernel<float><<<blocks, kThreads, 0, stream>>>(P, g, am, gD, err); break;
-    case kF16: grad_d_scatter_atomic_kernel<__half><<<blocks, kThreads, 0, stream>>>(P, g, am, gD, err); break;
-    default: grad_d_scatter_atomic_kernel<__nv_bfloat16><<<blocks, kThreads, 0, stream>>>(P, g, am, gD, err);
+    case kF32: return grad_d_typed<float>(P, g, am, gD, stream, err);
+    case kF16: return grad_d_typed<__half>(P, g, am, gD, stream, err);
+    default: return grad_d_typed<__nv_bfloat16>(P, g, am, gD, stream, err);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace lik

@@ -18,14 +18,14 @@
 //     S[128, T] = Qblock[128, dim] . Dtile[T, dim]^T      (fp32 in TMEM)
 // issued as dim/16 tcgen05.mma (kind::f16, M=128, N=T, K=16).
 //
-// Warp roles (320 threads, one CTA per SM, persistent over work units):
+// Warp roles (576 threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: Q row blocks (2 buffers) and D tiles (S stages)
 //   warp 1      TMEM allocator + single-thread MMA issuer
-//   warps 2..9  epilogue: two warpgroups; warp w reads TMEM lanes
+//   warps 2..17 epilogue: four warpgroups; warp w reads TMEM lanes
 //               32*(w%4)..+31, i.e. one accumulator row per thread.  The
-//               warpgroups split each tile's 32-column chunks (even / odd),
-//               keep a running (max, argmax) per row, and merge at the end of
-//               every document.
+//               warpgroups split each tile's 32-column chunks (chunk c goes
+//               to group c % 4), keep a running (max, argmax) per row, and
+//               merge at the end of every document.
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the MMA of
 // tile t+1 overlaps the epilogue of tile t.
 //
@@ -48,7 +48,10 @@
 namespace lik {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
+constexpr int kEpiGroups = kEpiWarps / 4;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kChunksPerGroup = 2;     // 32-column chunks per tile per warpgroup (T <= 256)
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kAtomElems = 64;
@@ -72,7 +75,8 @@ struct Bars {
     uint64_t full_d[kMaxStages], empty_d[kMaxStages];
     uint64_t full_q[2], empty_q[2];
     uint64_t acc_full[2], acc_empty[2];
-    uint64_t xchg[2];   // document-end exchange between the two epilogue warpgroups (256)
+    uint64_t xfull;     // warpgroups 1..3 have published a document's (max, argmax)
+    uint64_t xfree;     // warpgroup 0 has read them
     uint64_t qsum[2];   // per-query sums inside warpgroup 0 (128)
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -80,10 +84,10 @@ struct Bars {
 };
 
 struct Exchange {
-    float m[2][kM];
-    int a[2][kM];
-    uint32_t any[2][4];
-    float part[2][kM];  // per-row terms or per-warp partial sums
+    float m[kEpiGroups - 1][kM];     // running max of warpgroups 1..3 at a document end
+    int a[kEpiGroups - 1][kM];
+    uint32_t any[kEpiGroups - 1][4];
+    float part[2][kM];               // per-row terms or per-warp partial sums (warpgroup 0)
 };
 
 __device__ __forceinline__ int ksteps_of_atom(int dim, int a) {
@@ -116,23 +120,61 @@ __device__ __forceinline__ void tournament(const float (&v)[N], float& best, int
     idx = k[0];
 }
 
-template <int N>
-__device__ __forceinline__ void chunk_best(uint32_t taddr, uint32_t mw, float& best, int& idx) {
-    uint32_t raw[N];
-    if constexpr (N == 32)
-        ptx::tmem_ld_32(taddr, raw);
-    else
-        ptx::tmem_ld_16(taddr, raw);
-    float v[N];
-    const uint32_t full = N == 32 ? 0xffffffffu : 0xffffu;
-    if ((mw & full) == full) {
+// Best (value, lowest index) of 16 consecutive accumulator columns; `mw`
+// holds the 16 column-validity bits (invalid columns never win).
+__device__ __forceinline__ void chunk_best16(uint32_t taddr, uint32_t mw, float& best, int& idx) {
+    uint32_t raw[16];
+    ptx::tmem_ld_16(taddr, raw);
+    float v[16];
+    if (mw == 0xffffu) {
 #pragma unroll
-        for (int t = 0; t < N; ++t) v[t] = __uint_as_float(raw[t]);
+        for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(raw[t]);
     } else {
 #pragma unroll
-        for (int t = 0; t < N; ++t) v[t] = ((mw >> t) & 1u) ? __uint_as_float(raw[t]) : -INFINITY;
+        for (int t = 0; t < 16; ++t) v[t] = ((mw >> t) & 1u) ? __uint_as_float(raw[t]) : -INFINITY;
     }
-    tournament<N>(v, best, idx);
+    tournament<16>(v, best, idx);
+}
+
+// Position in a CTA's sequence of (work unit, document, tile).
+struct Cursor {
+    int64_t u, d, d1;
+    int t;
+    bool valid;
+};
+
+__device__ __forceinline__ Cursor unit_cursor(const Params& p, int64_t u) {
+    Cursor c;
+    c.u = u;
+    c.t = 0;
+    c.valid = u < p.n_units;
+    c.d = (u / p.n_rb) * p.dpu;
+    c.d1 = c.d + p.dpu < p.Nd ? c.d + p.dpu : p.Nd;
+    return c;
+}
+
+__device__ __forceinline__ Cursor first_cursor(const Params& p) { return unit_cursor(p, blockIdx.x); }
+
+__device__ __forceinline__ Cursor next_cursor(const Params& p, Cursor c) {
+    if (!c.valid) return c;
+    if (++c.t < p.tiles_per_doc) return c;
+    c.t = 0;
+    if (++c.d < c.d1) return c;
+    return unit_cursor(p, c.u + gridDim.x);
+}
+
+// Mask bytes of this warpgroup's chunks of the cursor's tile, one per lane
+// (0 for columns past the tile or the document).
+__device__ __forceinline__ void prefetch_mask(const Params& p, const Cursor& c, int wg, int lane,
+                                              int nchunks, uint8_t (&out)[kChunksPerGroup]) {
+#pragma unroll
+    for (int k = 0; k < kChunksPerGroup; ++k) {
+        const int ch = wg + kEpiGroups * k;
+        const int col = ch * 32 + lane;
+        const int64_t j = static_cast<int64_t>(c.t) * p.T + col;
+        const bool in = c.valid && ch < nchunks && col < p.T && j < p.Ld;
+        out[k] = in ? (p.dmask ? p.dmask[c.d * p.Ld + j] : uint8_t(1)) : uint8_t(0);
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -157,10 +199,11 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), 8);
-            ptx::mbar_init(ptx::smem_u32(&bars->xchg[b]), 256);
+            ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), kEpiWarps);
             ptx::mbar_init(ptx::smem_u32(&bars->qsum[b]), 128);
         }
+        ptx::mbar_init(ptx::smem_u32(&bars->xfull), (kEpiWarps - 4) * 32);
+        ptx::mbar_init(ptx::smem_u32(&bars->xfree), 4 * 32);
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
         ptx::fence_mbar_init();
     }
@@ -173,7 +216,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
     ptx::tc_fence_after();
     const uint32_t tmem_base = bars->tmem_base;
 
-    const int64_t Lq = p.Lq, Ld = p.Ld;
+    const int64_t Lq = p.Lq;
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
@@ -265,8 +308,8 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         }
     } else {
         // ------------------------------------------------------ epilogue --
-        const int ew = warp - 2;            // 0..7
-        const int half = ew >> 2;           // warpgroup: even / odd chunks
+        const int ew = warp - 2;            // 0..kEpiWarps-1
+        const int wg = ew >> 2;             // warpgroup: chunks c with c % kEpiGroups == wg
         const int quarter = warp & 3;       // TMEM lane quarter of this warp
         const int r = quarter * 32 + lane;  // accumulator row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -275,80 +318,102 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         const int qloc = static_cast<int>(r / Lq);
         const int i = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
         int ab = 0, par = 0;
-        uint32_t aph = 0, xph0 = 0, xph1 = 0, sph0 = 0, sph1 = 0;
+        uint32_t aph = 0, xph = 0, sph0 = 0, sph1 = 0;
         bool ok = true;
-        for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-            const int rb = static_cast<int>(u % p.n_rb);
-            const int64_t d0 = (u / p.n_rb) * p.dpu;
-            const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
-            const int64_t q = static_cast<int64_t>(rb) * p.qpt + qloc;
-            const bool row_ok = r < qrows && q < p.Nq;
-            const bool qvalid = row_ok && (!p.qmask || p.qmask[q * Lq + i]);
-            for (int64_t d = d0; ok && d < d1; ++d) {
-                float m = -INFINITY;
-                int am = -1;
-                uint32_t any = 0;
-                const uint8_t* dm = p.dmask ? p.dmask + d * Ld : nullptr;
-                for (int t = 0; t < p.tiles_per_doc; ++t) {
-                    const int64_t jt = static_cast<int64_t>(t) * p.T;
-                    // mask words of this warpgroup's chunks, fetched before the accumulator is ready
-                    uint32_t mw[4];
+
+        // Flat cursor over this CTA's (unit, document, tile) sequence, so the
+        // document-mask bytes of the next tile can be loaded while the
+        // current tile is processed.
+        Cursor cur = first_cursor(p), nxt;
+        uint8_t pre[kChunksPerGroup], pre_next[kChunksPerGroup];
+        prefetch_mask(p, cur, wg, lane, nchunks, pre);
+        int64_t row_unit = -1;
+        int64_t q = 0;
+        bool row_ok = false, qvalid = false;
+        float m = -INFINITY;
+        int am = -1;
+        bool any = false;
+        while (ok && cur.valid) {
+            uint32_t mw[kChunksPerGroup];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = half + 2 * k;
-                        const int col = c * 32 + lane;
-                        const int64_t j = jt + col;
-                        const bool v = c < nchunks && col < p.T && j < Ld && (!dm || dm[j]);
-                        mw[k] = __ballot_sync(0xffffffffu, v);
+            for (int k = 0; k < kChunksPerGroup; ++k) mw[k] = __ballot_sync(0xffffffffu, pre[k] != 0);
+            nxt = next_cursor(p, cur);
+            prefetch_mask(p, nxt, wg, lane, nchunks, pre_next);
+            if (cur.u != row_unit) {
+                row_unit = cur.u;
+                const int rb = static_cast<int>(cur.u % p.n_rb);
+                q = static_cast<int64_t>(rb) * p.qpt + qloc;
+                row_ok = r < qrows && q < p.Nq;
+                qvalid = row_ok && (!p.qmask || p.qmask[q * Lq + i]);
+            }
+            if (cur.t == 0) {
+                m = -INFINITY;
+                am = -1;
+                any = false;
+            }
+#pragma unroll
+            for (int k = 0; k < kChunksPerGroup; ++k) any = any || (mw[k] != 0);
+
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
+            const int jt = cur.t * p.T;
+#pragma unroll
+            for (int k = 0; k < kChunksPerGroup; ++k) {
+                const int c = wg + kEpiGroups * k;
+                if (c >= nchunks || mw[k] == 0) continue;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t hw = (mw[k] >> (16 * h)) & 0xffffu;
+                    if (hw == 0 || c * 32 + 16 * h >= p.T) continue;
+                    float cb;
+                    int ci;
+                    chunk_best16(acc + c * 32 + 16 * h, hw, cb, ci);
+                    if (cb > m) {
+                        m = cb;
+                        am = jt + c * 32 + 16 * h + ci;
                     }
-                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[ab]));
+            if (++ab == 2) { ab = 0; aph ^= 1; }
+
+            if (cur.t == p.tiles_per_doc - 1) {
+                // ---- document end: merge the warpgroups' (max, argmax).
+                // Groups 1..3 publish (after group 0 has read the previous
+                // document's values); group 0 waits for them, then merges.
+                if (wg > 0) {
+                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfree), xph ^ 1, err);
                     ok = __all_sync(0xffffffffu, ok);
+                    xph ^= 1;
                     if (!ok) break;
-                    ptx::tc_fence_after();
-                    const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
+                    xc->m[wg - 1][r] = m;
+                    xc->a[wg - 1][r] = am;
+                    if (lane == 0) xc->any[wg - 1][quarter] = any ? 1u : 0u;
+                    ptx::mbar_arrive(ptx::smem_u32(&bars->xfull));
+                } else {
+                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull), xph, err);
+                    ok = __all_sync(0xffffffffu, ok);
+                    xph ^= 1;
+                    if (!ok) break;
+                }
+                if (wg == 0) {
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int c = half + 2 * k;
-                        if (c >= nchunks || mw[k] == 0) continue;
-                        any |= mw[k];
-                        float cb;
-                        int ci;
-                        if (p.T - c * 32 >= 32)
-                            chunk_best<32>(acc + c * 32, mw[k], cb, ci);
-                        else
-                            chunk_best<16>(acc + c * 32, mw[k], cb, ci);
-                        if (cb > m) {
-                            m = cb;
-                            am = static_cast<int>(jt) + c * 32 + ci;
+                    for (int g2 = 0; g2 < kEpiGroups - 1; ++g2) {
+                        any = any || xc->any[g2][quarter] != 0;
+                        const float m1 = xc->m[g2][r];
+                        const int a1 = xc->a[g2][r];
+                        if (m1 > m || (m1 == m && a1 >= 0 && (am < 0 || a1 < am))) {
+                            m = m1;
+                            am = a1;
                         }
                     }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[ab]));
-                    if (++ab == 2) { ab = 0; aph ^= 1; }
-                }
-                if (!ok) break;
-
-                // ---- document end: merge the two warpgroups' (max, argmax)
-                if (half == 1) {
-                    xc->m[par][r] = m;
-                    xc->a[par][r] = am;
-                    if (lane == 0) xc->any[par][quarter] = any;
-                }
-                ptx::mbar_arrive(ptx::smem_u32(&bars->xchg[par]));
-                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xchg[par]), par ? xph1 : xph0, err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (par) xph1 ^= 1; else xph0 ^= 1;
-                if (!ok) break;
-                if (half == 0) {
-                    const float m1 = xc->m[par][r];
-                    const int a1 = xc->a[par][r];
-                    if (m1 > m || (m1 == m && a1 >= 0 && (am < 0 || a1 < am))) {
-                        m = m1;
-                        am = a1;
-                    }
-                    const bool doc_any = (any | xc->any[par][quarter]) != 0;
-                    const float term = (doc_any && qvalid) ? m : 0.0f;
+                    ptx::mbar_arrive(ptx::smem_u32(&bars->xfree));
+                    const float term = (any && qvalid) ? m : 0.0f;
                     // per-query sum over the query's rows, in a fixed order
                     float total = 0.0f;
                     bool writer = false;
@@ -383,14 +448,17 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                             for (int64_t k = 0; k < Lq && r + k < kM; ++k) total += xc->part[par][r + k];
                     }
                     if (row_ok) {
-                        const int64_t pair = q * p.Nd + d;
-                        if (writer) p.scores[pair] = doc_any ? total : kEmptyDocScore;
-                        if (p.argmax) p.argmax[pair * Lq + i] = (doc_any && qvalid) ? am : -1;
+                        const int64_t pair = q * p.Nd + cur.d;
+                        if (writer) p.scores[pair] = any ? total : kEmptyDocScore;
+                        if (p.argmax) p.argmax[pair * Lq + i] = (any && qvalid) ? am : -1;
                     }
                 }
                 par ^= 1;
                 if (!ok) break;
             }
+            cur = nxt;
+#pragma unroll
+            for (int k = 0; k < kChunksPerGroup; ++k) pre[k] = pre_next[k];
         }
     }
 
