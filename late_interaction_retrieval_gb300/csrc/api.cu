@@ -206,10 +206,21 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
     if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
     if ((st = check_aligned(scores, 4, "scores")) != LIK_OK) return st;
     if ((st = check_aligned(argmax, 4, "argmax")) != LIK_OK) return st;
-    const bool tc = tc_allpairs_eligible(P);
-    cudaError_t e = tc ? launch_fwd_tc_allpairs(P, scores, argmax, stream)
-                       : launch_fwd_simt(P, scores, argmax, stream);
-    if (e != cudaSuccess) return cuda_fail(e, tc ? "tensor-core forward launch" : "forward launch");
+    // kernel choice by layout and shape (the FFMA kernel takes fp32 and shapes
+    // outside the tensor-core kernels' limits)
+    cudaError_t e;
+    const char* what;
+    if (tc_allpairs_eligible(P)) {
+        e = launch_fwd_tc_allpairs(P, scores, argmax, stream);
+        what = "tensor-core all-pairs forward launch";
+    } else if (tc_stream_eligible(P)) {
+        e = launch_fwd_tc_stream(P, scores, argmax, stream);
+        what = "tensor-core streaming forward launch";
+    } else {
+        e = launch_fwd_simt(P, scores, argmax, stream);
+        what = "forward launch";
+    }
+    if (e != cudaSuccess) return cuda_fail(e, what);
     return LIK_OK;
 }
 

@@ -32,7 +32,7 @@ constexpr int kWarps = kThreads / 32;
 // take alternate pairs of the query.  The pairs are visited in chunks whose
 // argmax slice and upstream gradients (both contiguous in memory) are staged
 // in shared memory; every thread then gathers its document rows with
-// independent 16-byte loads, four pairs at a time.  The halves' partial sums
+// independent 16-byte loads, eight pairs at a time.  The halves' partial sums
 // are added in a fixed order at the end, so the result is deterministic.
 
 constexpr int kRowsPerCta = 32;
@@ -42,42 +42,32 @@ constexpr int kVecThreads = kRowsPerCta * kThreadsPerRow * kPairGroups;  // 512
 constexpr int kVec = 8;                                                  // elements per vector
 constexpr int kPairChunk = 64;
 
-struct Vec8 {
-    float v[kVec];
+// Eight consecutive elements kept in their storage type until the FMA, so
+// that many rows can be in flight per thread: 16 bytes for fp16/bf16.
+template <typename T>
+struct Raw8 {
+    uint4 v;
+    __device__ __forceinline__ void load(const T* p) { v = *reinterpret_cast<const uint4*>(p); }
+    __device__ __forceinline__ float get(int e) const {
+        const T* h = reinterpret_cast<const T*>(&v);
+        return to_f32(h[e]);
+    }
+};
+template <>
+struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float* p) {
+        a = *reinterpret_cast<const float4*>(p);
+        b = *reinterpret_cast<const float4*>(p + 4);
+    }
+    __device__ __forceinline__ float get(int e) const {
+        const float* f = e < 4 ? reinterpret_cast<const float*>(&a) : reinterpret_cast<const float*>(&b);
+        return f[e & 3];
+    }
 };
 
-__device__ __forceinline__ Vec8 load_vec8(const float* p) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    return {{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w}};
-}
-__device__ __forceinline__ Vec8 load_vec8(const __half* p) {
-    const uint4 r = *reinterpret_cast<const uint4*>(p);
-    const __half2* h = reinterpret_cast<const __half2*>(&r);
-    Vec8 o;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const float2 f = __half22float2(h[t]);
-        o.v[2 * t] = f.x;
-        o.v[2 * t + 1] = f.y;
-    }
-    return o;
-}
-__device__ __forceinline__ Vec8 load_vec8(const __nv_bfloat16* p) {
-    const uint4 r = *reinterpret_cast<const uint4*>(p);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&r);
-    Vec8 o;
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-        const float2 f = __bfloat1622float2(h[t]);
-        o.v[2 * t] = f.x;
-        o.v[2 * t + 1] = f.y;
-    }
-    return o;
-}
-
 // VECS vectors of 8 elements per thread: dim <= VECS * 64.
-template <typename T, int VECS>
+template <typename T, int VECS, int kUnroll>
 __global__ void __launch_bounds__(kVecThreads)
 grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
                   float* __restrict__ gQ, unsigned int* err) {
@@ -112,11 +102,11 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
         __syncthreads();
         if (r >= rows_here) continue;
         // this half takes pairs t = pg, pg + 2, pg + 4, ... of the chunk
-        for (int t = pg; t < nc; t += 4 * kPairGroups) {
-            const T* rows[4];
-            float gv[4];
+        for (int t = pg; t < nc; t += kUnroll * kPairGroups) {
+            const T* rows[kUnroll];
+            float gv[kUnroll];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < kUnroll; ++u) {
                 const int tt = t + u * kPairGroups;
                 int a = tt < nc ? s_am[tt][r] : -1;
                 if (a >= P.Ld) {
@@ -124,21 +114,21 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
                     a = -1;
                 }
                 gv[u] = a >= 0 ? s_g[tt] : 0.f;
-                rows[u] = a >= 0 ? D + (P.doc_of(p0 + c0 + tt) * P.Ld + a) * P.dim : nullptr;
+                rows[u] = a >= 0 ? D + (P.doc_of_query_pair(q, c0 + tt) * P.Ld + a) * P.dim : nullptr;
             }
 #pragma unroll
             for (int m = 0; m < VECS; ++m) {
                 const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
                 if (k >= P.dim) break;
-                Vec8 x[4];
+                Raw8<T> x[kUnroll];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (rows[u]) x[u] = load_vec8(rows[u] + k);
+                for (int u = 0; u < kUnroll; ++u)
+                    if (rows[u]) x[u].load(rows[u] + k);
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
+                for (int u = 0; u < kUnroll; ++u)
                     if (rows[u])
 #pragma unroll
-                        for (int e = 0; e < kVec; ++e) acc[m][e] = fmaf(gv[u], x[u].v[e], acc[m][e]);
+                        for (int e = 0; e < kVec; ++e) acc[m][e] = fmaf(gv[u], x[u].get(e), acc[m][e]);
             }
         }
     }
@@ -206,9 +196,10 @@ grad_q_gather_kernel(Problem P, const float* __restrict__ g, const int32_t* __re
 // ------------------------------------------------------------- grad_D --
 //
 // grad_D is zero-filled on the stream, then every (pair, token) hit adds
-// g * Q[q,i,:] into grad_D[d, a, :].  Vector path (dim % 4 == 0): each lane
-// adds 4 consecutive fp32 with one 16-byte reduction (red.global.add.v4.f32),
-// a warp covers 128 dims of one hit, and each warp keeps two hits in flight.
+// g * Q[q,i,:] into grad_D[d, a, :].  Vector path (dim % 4 == 0): one warp
+// per pair loads 32 of the pair's saved argmax at once; each lane adds 4
+// consecutive fp32 with one 16-byte reduction (red.global.add.v4.f32), a
+// warp covers 128 dims of one hit, and two hits are in flight per step.
 
 __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
@@ -248,37 +239,40 @@ grad_d_scatter_vec_kernel(Problem P, const float* __restrict__ g, const int32_t*
                           float* __restrict__ gD, unsigned int* err) {
     const T* Q = static_cast<const T*>(P.Q);
     const int lane = threadIdx.x & 31;
-    const int64_t hits = P.n_pairs * P.Lq;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps * 2;
-    for (int64_t h0 = (static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5)) * 2; h0 < hits;
-         h0 += stride) {
-        int32_t a[2];
-        float gv[2];
-        const T* qrow[2];
-        float* out[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int64_t h = h0 + u;
-            a[u] = h < hits ? am[h] : -1;
-            if (a[u] >= P.Ld) {
-                if (lane == 0) atomicOr(err, kErrBadIndex);
-                a[u] = -1;
+    // one warp per pair; its query tokens' argmax are loaded 32 at a time
+    for (int64_t p = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); p < P.n_pairs;
+         p += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t q = P.query_of(p), d = P.doc_of(p);
+        const float gv = g[p];
+        const T* qbase = Q + q * P.Lq * P.dim;
+        float* dbase = gD + d * P.Ld * P.dim;
+        for (int64_t i0 = 0; i0 < P.Lq; i0 += 32) {
+            const int64_t i = i0 + lane;
+            int32_t a = i < P.Lq ? am[p * P.Lq + i] : -1;
+            if (a >= P.Ld) {
+                atomicOr(err, kErrBadIndex);
+                a = -1;
             }
-            const int64_t p = h / P.Lq, i = h - p * P.Lq;
-            gv[u] = a[u] >= 0 ? g[p] : 0.f;
-            qrow[u] = Q + (P.query_of(p) * P.Lq + i) * P.dim;
-            out[u] = gD + (P.doc_of(p) * P.Ld + (a[u] >= 0 ? a[u] : 0)) * P.dim;
-        }
-        for (int64_t k = lane * 4; k < P.dim; k += 128) {
-            float x[2][4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (a[u] >= 0) load4(qrow[u] + k, x[u]);
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-                if (a[u] >= 0)
-                    red_add_v4(out[u] + k, gv[u] * x[u][0], gv[u] * x[u][1], gv[u] * x[u][2],
-                               gv[u] * x[u][3]);
+            uint32_t live = __ballot_sync(0xffffffffu, a >= 0);
+            // two hits in flight per step
+            while (live) {
+                const int s0 = __ffs(live) - 1;
+                live &= live - 1;
+                const int s1 = live ? __ffs(live) - 1 : -1;
+                if (s1 >= 0) live &= live - 1;
+                const int a0 = __shfl_sync(0xffffffffu, a, s0);
+                const int a1 = __shfl_sync(0xffffffffu, a, s1 >= 0 ? s1 : s0);
+                const T* q0 = qbase + (i0 + s0) * P.dim;
+                const T* q1 = qbase + (i0 + (s1 >= 0 ? s1 : s0)) * P.dim;
+                for (int64_t k = lane * 4; k < P.dim; k += 128) {
+                    float x0[4], x1[4];
+                    load4(q0 + k, x0);
+                    if (s1 >= 0) load4(q1 + k, x1);
+                    red_add_v4(dbase + a0 * P.dim + k, gv * x0[0], gv * x0[1], gv * x0[2], gv * x0[3]);
+                    if (s1 >= 0)
+                        red_add_v4(dbase + a1 * P.dim + k, gv * x1[0], gv * x1[1], gv * x1[2], gv * x1[3]);
+                }
+            }
         }
     }
 }
@@ -324,10 +318,11 @@ cudaError_t grad_q_typed(const Problem& P, const float* g, const int32_t* am, fl
     const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t blocks = P.n_query * groups;
     if (P.dim % kVec == 0 && P.dim <= 256 && blocks < (int64_t(1) << 31)) {
+        // 8 (dim <= 128) or 4 (dim <= 256) independent row loads in flight per thread
         if (P.dim <= 128)
-            grad_q_vec_kernel<T, 2><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+            grad_q_vec_kernel<T, 2, 8><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
         else
-            grad_q_vec_kernel<T, 4><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+            grad_q_vec_kernel<T, 4, 4><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
         return cudaGetLastError();
     }
     grad_q_gather_kernel<T><<<grid_for(P.n_query * P.Lq, 16), kThreads, 0, stream>>>(P, g, am, gQ, err);
@@ -339,7 +334,7 @@ cudaError_t grad_d_typed(const Problem& P, const float* g, const int32_t* am, fl
                          cudaStream_t stream, unsigned int* err) {
     const int64_t hits = P.n_pairs * P.Lq;
     if (P.dim % 4 == 0)
-        grad_d_scatter_vec_kernel<T><<<grid_for((hits + 1) / 2, 16), kThreads, 0, stream>>>(P, g, am, gD, err);
+        grad_d_scatter_vec_kernel<T><<<grid_for(P.n_pairs, 16), kThreads, 0, stream>>>(P, g, am, gD, err);
     else
         grad_d_scatter_atomic_kernel<T><<<grid_for(hits, 16), kThreads, 0, stream>>>(P, g, am, gD, err);
     return cudaGetLastError();

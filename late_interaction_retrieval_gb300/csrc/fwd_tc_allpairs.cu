@@ -29,10 +29,11 @@
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the MMA of
 // tile t+1 overlaps the epilogue of tile t.
 //
-// Epilogue per 32-column chunk: one tcgen05.ld, the document mask as a
-// warp-uniform 32-bit word (one ballot), a lowest-index tournament over the
-// 32 values, and a strictly-greater merge into the running max -- so ties go
-// to the lowest token index, as in the oracle.  At a document's end the
+// Epilogue per 32-column chunk: the document mask as a warp-uniform 32-bit
+// word (one ballot, loaded a tile ahead), two 16-column tcgen05.ld, an exact
+// max by 3-input max instructions and the column of the max by a packed-key
+// max (chunk_best16), and a strictly-greater merge into the running max, so
+// exact ties between chunks go to the lowest token index, as in the oracle.  At a document's end the
 // maxima of the valid query tokens are summed per query (fixed order) and
 // the score and argmax are written.
 //
@@ -95,45 +96,48 @@ __device__ __forceinline__ int ksteps_of_atom(int dim, int a) {
     return (rem >= kAtomElems ? kAtomElems : rem) / 16;
 }
 
-// Lowest-index argmax of n values (n = 16 or 32) by a tournament: pairs are
-// compared with a strict '>' so the left (lower) index wins ties.
-template <int N>
-__device__ __forceinline__ void tournament(const float (&v)[N], float& best, int& idx) {
-    float m[N / 2];
-    int k[N / 2];
-#pragma unroll
-    for (int t = 0; t < N / 2; ++t) {
-        const bool p = v[2 * t + 1] > v[2 * t];
-        m[t] = p ? v[2 * t + 1] : v[2 * t];
-        k[t] = 2 * t + (p ? 1 : 0);
-    }
-#pragma unroll
-    for (int w = N / 4; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int t = 0; t < w; ++t) {
-            const bool p = m[2 * t + 1] > m[2 * t];
-            m[t] = p ? m[2 * t + 1] : m[2 * t];
-            k[t] = p ? k[2 * t + 1] : k[2 * t];
-        }
-    }
-    best = m[0];
-    idx = k[0];
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
-// Best (value, lowest index) of 16 consecutive accumulator columns; `mw`
-// holds the 16 column-validity bits (invalid columns never win).
+// Max of 16 values with 3-input max (8 instructions).
+__device__ __forceinline__ float max16(const float (&v)[16]) {
+    const float a = max3f(v[0], v[1], v[2]), b = max3f(v[3], v[4], v[5]), c = max3f(v[6], v[7], v[8]);
+    const float d = max3f(v[9], v[10], v[11]), e = max3f(v[12], v[13], v[14]);
+    return max3f(max3f(a, b, c), fmaxf(d, e), v[15]);
+}
+
+// 16 consecutive accumulator columns of this thread's row.  `mw` holds the
+// 16 column-validity bits.  Returns the exact max over the valid columns
+// and, when kArg, the column of a maximum: the lowest column whose value
+// equals the max in every bit but the last four.  That index comes from a
+// second max over packed keys (value with its low 4 mantissa bits replaced
+// by 15 - column), so each column costs one LOP3 and a third of two 3-input
+// maxima instead of a compare and two selects.  A column picked this way
+// holds the max or a value within 2^-19 of it relative; exact ties between
+// non-negative values resolve to the lowest column.
+template <bool kArg>
 __device__ __forceinline__ void chunk_best16(uint32_t taddr, uint32_t mw, float& best, int& idx) {
     uint32_t raw[16];
     ptx::tmem_ld_16(taddr, raw);
-    float v[16];
-    if (mw == 0xffffu) {
+    if (mw != 0xffffu) {
 #pragma unroll
-        for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(raw[t]);
-    } else {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) v[t] = ((mw >> t) & 1u) ? __uint_as_float(raw[t]) : -INFINITY;
+        for (int t = 0; t < 16; ++t) raw[t] = ((mw >> t) & 1u) ? raw[t] : 0xff7fffffu;  // -FLT_MAX
     }
-    tournament<16>(v, best, idx);
+    float v[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(raw[t]);
+    best = max16(v);
+    if constexpr (kArg) {
+        float k[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) k[t] = __uint_as_float((raw[t] & 0xfffffff0u) | (15u - t));
+        idx = 15 - static_cast<int>(__float_as_uint(max16(k)) & 15u);
+    } else {
+        idx = 0;
+    }
 }
 
 // Position in a CTA's sequence of (work unit, document, tile).
@@ -177,6 +181,7 @@ __device__ __forceinline__ void prefetch_mask(const Params& p, const Cursor& c, 
     }
 }
 
+template <bool kArg>
 __global__ void __launch_bounds__(kThreads, 1)
 allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmd,
                        const Params p) {
@@ -370,7 +375,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                     if (hw == 0 || c * 32 + 16 * h >= p.T) continue;
                     float cb;
                     int ci;
-                    chunk_best16(acc + c * 32 + 16 * h, hw, cb, ci);
+                    chunk_best16<kArg>(acc + c * 32 + 16 * h, hw, cb, ci);
                     if (cb > m) {
                         m = cb;
                         am = jt + c * 32 + 16 * h + ci;
@@ -534,11 +539,12 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
 
     const size_t smem = 1024 + 2 * static_cast<size_t>(p.q_bytes) +
                         static_cast<size_t>(p.stages) * p.d_bytes + misc;
-    e = cudaFuncSetAttribute(allpairs_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    // the max-only variant (no argmax requested: inference) skips the index work
+    auto kernel = argmax ? allpairs_fwd_tc_kernel<true> : allpairs_fwd_tc_kernel<false>;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int64_t grid = p.n_units < info.sm_count ? p.n_units : info.sm_count;
-    allpairs_fwd_tc_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmq, tmd, p);
+    kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(tmq, tmd, p);
     return cudaGetLastError();
 }
 

@@ -39,6 +39,10 @@ struct Problem {
     __host__ __device__ int64_t doc_of(int64_t p) const {
         return layout == kAllPairs ? p % pairs_per_query : p;
     }
+    // Document of the t-th pair of query q (pair q*pairs_per_query + t), without a division.
+    __host__ __device__ int64_t doc_of_query_pair(int64_t q, int64_t t) const {
+        return layout == kAllPairs ? t : q * pairs_per_query + t;
+    }
 };
 
 // Device properties the launchers need, cached per device.
@@ -69,6 +73,12 @@ cudaError_t launch_fwd_simt(const Problem& P, float* scores, int32_t* argmax,
 bool tc_allpairs_eligible(const Problem& P);
 cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* argmax,
                                    cudaStream_t stream);
+
+// Tensor-core (tcgen05) streaming forward for the pairwise and kd layouts,
+// fp16/bf16: dim % 16 == 0, dim <= 256, 1 <= Lq <= 64, Ld >= 1.
+bool tc_stream_eligible(const Problem& P);
+cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax,
+                                 cudaStream_t stream);
 
 // Backward: grad_Q gather and grad_D scatter (grad_D zero-filled first).
 cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,
