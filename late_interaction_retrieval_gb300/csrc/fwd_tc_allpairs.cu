@@ -23,17 +23,17 @@
 //   warp 1      TMEM allocator + single-thread MMA issuer
 //   warps 2..17 epilogue: four warpgroups; warp w reads TMEM lanes
 //               32*(w%4)..+31, i.e. one accumulator row per thread.  The
-//               warpgroups split each tile's 32-column chunks (chunk c goes
-//               to group c % 4), keep a running (max, argmax) per row, and
-//               merge at the end of every document.
+//               warpgroups split each tile's 16-column units round-robin
+//               (unit u goes to group u % 4), keep a running (max, argmax)
+//               per row, and merge at the end of every document.
 // The accumulator is double-buffered in TMEM (2 x 256 columns), so the MMA of
 // tile t+1 overlaps the epilogue of tile t.
 //
-// Epilogue per 32-column chunk: the document mask as a warp-uniform 32-bit
-// word (one ballot, loaded a tile ahead), two 16-column tcgen05.ld, an exact
-// max by 3-input max instructions and the column of the max by a packed-key
-// max (chunk_best16), and a strictly-greater merge into the running max, so
-// exact ties between chunks go to the lowest token index, as in the oracle.  At a document's end the
+// Epilogue per 16-column unit: the document mask as warp-uniform bits (one
+// ballot per two units, loaded a tile ahead), one tcgen05.ld, an exact max
+// by 3-input max instructions and the column of the max by a packed-key max
+// (chunk_best16), and a strictly-greater merge into the running max, so
+// exact ties between units go to the lowest token index, as in the oracle.  At a document's end the
 // maxima of the valid query tokens are summed per query (fixed order) and
 // the score and argmax are written.
 //
@@ -52,7 +52,7 @@ namespace {
 constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kChunksPerGroup = 2;     // 32-column chunks per tile per warpgroup (T <= 256)
+constexpr int kUnitsPerGroup = 4;      // 16-column units per tile per warpgroup (T <= 256)
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kAtomElems = 64;
@@ -167,17 +167,20 @@ __device__ __forceinline__ Cursor next_cursor(const Params& p, Cursor c) {
     return unit_cursor(p, c.u + gridDim.x);
 }
 
-// Mask bytes of this warpgroup's chunks of the cursor's tile, one per lane
-// (0 for columns past the tile or the document).
+// Mask bytes of this warpgroup's 16-column units of the cursor's tile.
+// Step m covers units wg + 4*(2m) (lanes 0..15) and wg + 4*(2m+1) (lanes
+// 16..31), one column per lane; 0 past the tile or the document.
 __device__ __forceinline__ void prefetch_mask(const Params& p, const Cursor& c, int wg, int lane,
-                                              int nchunks, uint8_t (&out)[kChunksPerGroup]) {
+                                              uint8_t (&out)[kUnitsPerGroup / 2]) {
+    const uint8_t* dm = p.dmask ? p.dmask + c.d * p.Ld : nullptr;
+    const int lim = c.valid ? static_cast<int>(p.Ld - static_cast<int64_t>(c.t) * p.T) : 0;
+    const int jt = c.t * p.T;
 #pragma unroll
-    for (int k = 0; k < kChunksPerGroup; ++k) {
-        const int ch = wg + kEpiGroups * k;
-        const int col = ch * 32 + lane;
-        const int64_t j = static_cast<int64_t>(c.t) * p.T + col;
-        const bool in = c.valid && ch < nchunks && col < p.T && j < p.Ld;
-        out[k] = in ? (p.dmask ? p.dmask[c.d * p.Ld + j] : uint8_t(1)) : uint8_t(0);
+    for (int m = 0; m < kUnitsPerGroup / 2; ++m) {
+        const int unit = wg + kEpiGroups * (2 * m + (lane >> 4));
+        const int col = unit * 16 + (lane & 15);
+        const bool in = col < p.T && col < lim;
+        out[m] = in ? (dm ? dm[jt + col] : uint8_t(1)) : uint8_t(0);
     }
 }
 
@@ -318,7 +321,6 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         const int quarter = warp & 3;       // TMEM lane quarter of this warp
         const int r = quarter * 32 + lane;  // accumulator row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const int nchunks = (p.T + 31) >> 5;
         const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
         const int qloc = static_cast<int>(r / Lq);
         const int i = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
@@ -330,8 +332,8 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         // document-mask bytes of the next tile can be loaded while the
         // current tile is processed.
         Cursor cur = first_cursor(p), nxt;
-        uint8_t pre[kChunksPerGroup], pre_next[kChunksPerGroup];
-        prefetch_mask(p, cur, wg, lane, nchunks, pre);
+        uint8_t pre[kUnitsPerGroup / 2], pre_next[kUnitsPerGroup / 2];
+        prefetch_mask(p, cur, wg, lane, pre);
         int64_t row_unit = -1;
         int64_t q = 0;
         bool row_ok = false, qvalid = false;
@@ -339,11 +341,11 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         int am = -1;
         bool any = false;
         while (ok && cur.valid) {
-            uint32_t mw[kChunksPerGroup];
+            uint32_t mw[kUnitsPerGroup / 2];
 #pragma unroll
-            for (int k = 0; k < kChunksPerGroup; ++k) mw[k] = __ballot_sync(0xffffffffu, pre[k] != 0);
+            for (int k = 0; k < kUnitsPerGroup / 2; ++k) mw[k] = __ballot_sync(0xffffffffu, pre[k] != 0);
             nxt = next_cursor(p, cur);
-            prefetch_mask(p, nxt, wg, lane, nchunks, pre_next);
+            prefetch_mask(p, nxt, wg, lane, pre_next);
             if (cur.u != row_unit) {
                 row_unit = cur.u;
                 const int rb = static_cast<int>(cur.u % p.n_rb);
@@ -357,7 +359,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 any = false;
             }
 #pragma unroll
-            for (int k = 0; k < kChunksPerGroup; ++k) any = any || (mw[k] != 0);
+            for (int k = 0; k < kUnitsPerGroup / 2; ++k) any = any || (mw[k] != 0);
 
             ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
             ok = __all_sync(0xffffffffu, ok);
@@ -366,20 +368,16 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
             const int jt = cur.t * p.T;
 #pragma unroll
-            for (int k = 0; k < kChunksPerGroup; ++k) {
-                const int c = wg + kEpiGroups * k;
-                if (c >= nchunks || mw[k] == 0) continue;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t hw = (mw[k] >> (16 * h)) & 0xffffu;
-                    if (hw == 0 || c * 32 + 16 * h >= p.T) continue;
-                    float cb;
-                    int ci;
-                    chunk_best16<kArg>(acc + c * 32 + 16 * h, hw, cb, ci);
-                    if (cb > m) {
-                        m = cb;
-                        am = jt + c * 32 + 16 * h + ci;
-                    }
+            for (int k = 0; k < kUnitsPerGroup; ++k) {
+                const int unit = wg + kEpiGroups * k;
+                const uint32_t hw = (mw[k >> 1] >> (16 * (k & 1))) & 0xffffu;
+                if (hw == 0) continue;  // no valid column (or past the tile)
+                float cb;
+                int ci;
+                chunk_best16<kArg>(acc + unit * 16, hw, cb, ci);
+                if (cb > m) {
+                    m = cb;
+                    am = jt + unit * 16 + ci;
                 }
             }
             ptx::tc_fence_before();
@@ -463,7 +461,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             }
             cur = nxt;
 #pragma unroll
-            for (int k = 0; k < kChunksPerGroup; ++k) pre[k] = pre_next[k];
+            for (int k = 0; k < kUnitsPerGroup / 2; ++k) pre[k] = pre_next[k];
         }
     }
 

@@ -32,14 +32,16 @@
 //               follows: data tiles, one end-of-document record per pair, and
 //               an end-of-stream record.
 //   warp 1      TMEM allocator + single-thread MMA issuer (4 accumulators).
-//   warps 2..   epilogue, one group of 4 warps per 32 query tokens.  Each
-//               thread owns one accumulator lane (document token) and keeps
-//               a running (max, argmax) for each of its group's 32 query
+//   update warps  one group of 4 warps per 32 query tokens.  Each thread
+//               owns one accumulator lane (document token) and keeps a
+//               running (max, argmax) for each of its group's 32 query
 //               tokens in registers across the document's tiles.  At the end
-//               of a document the group transposes those through shared
-//               memory, reduces over the 128 lanes (lowest token index on
-//               ties), sums the valid query tokens in a fixed order, and
-//               writes the score and argmax.
+//               of a document it dumps that state to shared memory (double-
+//               buffered) and goes straight on with the next document.
+//   reducer warps (4) reduce each dumped document over its 128 lanes per
+//               query token (lowest token index on ties), sum the valid
+//               query tokens in a fixed order, and write the score and
+//               argmax, while the stream continues.
 // Every mbarrier wait is bounded; on expiry the kernel flags the library's
 // error word, drains its own loads and MMAs, frees TMEM and returns.
 #include <cfloat>
@@ -57,7 +59,7 @@ constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 8;
 constexpr int kAccBufs = 4;
 constexpr int kRing = 16;           // tile records in flight
-constexpr int kMaxGroups = 2;       // Lq <= 64
+constexpr int kMaxGroups = 1;       // Lq <= 32 (the double-buffered dump fits shared memory)
 
 enum : int { kRecTile = 0, kRecDocEnd = 1, kRecStop = 2 };
 
@@ -93,20 +95,35 @@ struct Bars {
     uint64_t full_q[2], empty_q[2];
     uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
     uint64_t rec_full[kRing], rec_empty[kRing];
-    uint64_t red1[kMaxGroups][2], red2[kMaxGroups][2], grp_sum[2];
+    uint64_t dump_full[2], dump_empty[2];  // update warps -> reducer warps
+    uint64_t red_mid;                      // reducer warps: partials written
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t pad;
 };
 
+// Per-document state handed from the update warps to the reducer warps
+// (double-buffered): every lane's running (max, argmax) per query token,
+// rows padded to 33 words so both the row-wise writes and the column-wise
+// reads are free of bank conflicts.
+struct Dump {
+    float m[kRows][33];
+    int a[kRows][33];
+};
+
+struct DumpInfo {
+    int64_t pair;
+    int nonempty;
+    int stop;
+};
+
 struct Shared {
     Rec rec[kRing];
     StageMeta meta[kMaxStages];
-    float red_m[kMaxGroups][kRows][33];
-    int red_a[kMaxGroups][kRows][33];
-    float part_m[kMaxGroups][4][32];
-    int part_a[kMaxGroups][4][32];
-    float gsum[2][kMaxGroups];
+    DumpInfo info[2];
+    float part_m[4][32];
+    int part_a[4][32];
+    float gsum[kMaxGroups];
 };
 
 __device__ __forceinline__ int64_t doc_of(const Params& p, int64_t pair) {
@@ -133,7 +150,7 @@ __device__ __forceinline__ void load_tile_mask(const Params& p, int64_t d, int64
     }
 }
 
-__global__ void __launch_bounds__(32 * (2 + 4 * kMaxGroups), 1)
+__global__ void __launch_bounds__(32 * (2 + 4 * kMaxGroups + 4), 1)
 stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmd,
                      const Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -142,6 +159,7 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
     uint8_t* dbuf = smem + 2 * p.q_bytes;          // stages x d_bytes
     Bars* bars = reinterpret_cast<Bars*>(dbuf + p.stages * p.d_bytes);
     Shared* sh = reinterpret_cast<Shared*>(bars + 1);
+    Dump* dump = reinterpret_cast<Dump*>(sh + 1);  // [2][groups]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     unsigned int* err = p.err;
@@ -159,11 +177,8 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->grp_sum[b]), 32 * 4 * p.groups);
-            for (int g = 0; g < kMaxGroups; ++g) {
-                ptx::mbar_init(ptx::smem_u32(&bars->red1[g][b]), 128);
-                ptx::mbar_init(ptx::smem_u32(&bars->red2[g][b]), 128);
-            }
+            ptx::mbar_init(ptx::smem_u32(&bars->dump_full[b]), 32 * 4 * p.groups);
+            ptx::mbar_init(ptx::smem_u32(&bars->dump_empty[b]), 128);
         }
         for (int b = 0; b < kAccBufs; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
@@ -173,6 +188,7 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             ptx::mbar_init(ptx::smem_u32(&bars->rec_full[r]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->rec_empty[r]), 4 * p.groups);
         }
+        ptx::mbar_init(ptx::smem_u32(&bars->red_mid), 128);
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
         ptx::fence_mbar_init();
     }
@@ -355,16 +371,15 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, err);
         }
     } else if (warp < 2 + 4 * p.groups) {
-        // ------------------------------------------------------ epilogue --
+        // ------------------------------------------------ update warps --
         const int ew = warp - 2;
         const int g = ew >> 2;                // query-token group: columns 32g .. 32g+31
         const int quarter = warp & 3;         // TMEM lane quarter
         const int r = quarter * 32 + lane;    // tile row = document token jt + r
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int col0 = 32 * g;
-        int ri = 0, ab = 0, par = 0;
-        uint32_t rph = 0, aph = 0;
-        uint32_t r1ph[2] = {0, 0}, r2ph[2] = {0, 0}, gph[2] = {0, 0};
+        int ri = 0, ab = 0, db = 0;
+        uint32_t rph = 0, aph = 0, dph = 0;
         bool ok = true;
         float m[32];
         int am[32];
@@ -381,7 +396,6 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->rec_empty[ri]));
             if (++ri == kRing) { ri = 0; rph ^= 1; }
-            if (rec.kind == kRecStop) break;
             if (rec.kind == kRecTile) {
                 ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
                 ok = __all_sync(0xffffffffu, ok);
@@ -406,73 +420,98 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
                 }
                 continue;
             }
-            // ---- end of a document: reduce over the 128 lanes per query token
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                sh->red_m[g][r][c] = m[c];
-                sh->red_a[g][r][c] = am[c];
-                m[c] = -INFINITY;
-                am[c] = -1;
-            }
-            ptx::mbar_arrive(ptx::smem_u32(&bars->red1[g][par]));
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->red1[g][par]), r1ph[par], err);
+            // end of a document (or of the stream): hand the state to the reducer
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dump_empty[db]), dph ^ 1, err);
             ok = __all_sync(0xffffffffu, ok);
-            r1ph[par] ^= 1;
             if (!ok) break;
-            {
-                // thread (quarter, lane): column `lane` over rows 32*quarter .. +31, ascending
+            if (rec.kind == kRecDocEnd) {
+                Dump& dd = dump[db * p.groups + g];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    dd.m[r][c] = m[c];
+                    dd.a[r][c] = am[c];
+                    m[c] = -INFINITY;
+                    am[c] = -1;
+                }
+            }
+            if (g == 0 && r == 0) {
+                sh->info[db].pair = rec.pair;
+                sh->info[db].nonempty = rec.nonempty;
+                sh->info[db].stop = rec.kind == kRecStop ? 1 : 0;
+            }
+            ptx::mbar_arrive(ptx::smem_u32(&bars->dump_full[db]));
+            if (++db == 2) { db = 0; dph ^= 1; }
+            if (rec.kind == kRecStop) break;
+        }
+    } else if (warp < 2 + 4 * p.groups + 4) {
+        // ----------------------------------------------- reducer warps --
+        // For each document: every (quarter, lane) thread takes query token
+        // `lane` over rows 32*quarter .. +31 in ascending order, the four
+        // partials are merged in row order (lowest token index on ties), the
+        // valid tokens' maxima are summed per group in a fixed order, then
+        // the groups' sums in group order.
+        const int quarter = (warp - 2 - 4 * p.groups);
+        int db = 0;
+        uint32_t dph = 0, mph = 0;
+        bool ok = true;
+        while (ok) {
+            ok = ptx::mbar_wait(ptx::smem_u32(&bars->dump_full[db]), dph, err);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const DumpInfo info = sh->info[db];
+            if (info.stop) break;
+            const int64_t pair = info.pair;
+            const int64_t qi = query_of(p, pair);
+            float total = 0.0f;
+            for (int g = 0; g < p.groups; ++g) {
+                const Dump& dd = dump[db * p.groups + g];
                 float bm = -INFINITY;
                 int ba = -1;
                 for (int rr = 32 * quarter; rr < 32 * quarter + 32; ++rr) {
-                    const float v = sh->red_m[g][rr][lane];
+                    const float v = dd.m[rr][lane];
                     if (v > bm) {
                         bm = v;
-                        ba = sh->red_a[g][rr][lane];
+                        ba = dd.a[rr][lane];
                     }
                 }
-                sh->part_m[g][quarter][lane] = bm;
-                sh->part_a[g][quarter][lane] = ba;
-            }
-            ptx::mbar_arrive(ptx::smem_u32(&bars->red2[g][par]));
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->red2[g][par]), r2ph[par], err);
-            ok = __all_sync(0xffffffffu, ok);
-            r2ph[par] ^= 1;
-            if (!ok) break;
-            const int64_t pair = rec.pair;
-            const int64_t qi = query_of(p, pair);
-            float term = 0.0f;
-            if (quarter == 0) {
-                float bm = -INFINITY;
-                int ba = -1;
+                sh->part_m[quarter][lane] = bm;
+                sh->part_a[quarter][lane] = ba;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->red_mid));
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->red_mid), mph, err);
+                ok = __all_sync(0xffffffffu, ok);
+                mph ^= 1;
+                if (!ok) break;
+                if (quarter == 0) {
+                    float cm = -INFINITY;
+                    int ca = -1;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float v = sh->part_m[g][w][lane];
-                    if (v > bm) {
-                        bm = v;
-                        ba = sh->part_a[g][w][lane];
+                    for (int w = 0; w < 4; ++w) {
+                        const float v = sh->part_m[w][lane];
+                        if (v > cm) {
+                            cm = v;
+                            ca = sh->part_a[w][lane];
+                        }
                     }
-                }
-                const int i = col0 + lane;
-                const bool qvalid = i < p.Lq && (!p.qmask || p.qmask[qi * p.Lq + i]);
-                const bool live = rec.nonempty && qvalid;
-                if (i < p.Lq && p.argmax) p.argmax[pair * p.Lq + i] = live ? ba : -1;
-                term = live ? bm : 0.0f;
+                    const int i = 32 * g + lane;
+                    const bool qvalid = i < p.Lq && (!p.qmask || p.qmask[qi * p.Lq + i]);
+                    const bool live = info.nonempty && qvalid;
+                    if (i < p.Lq && p.argmax) p.argmax[pair * p.Lq + i] = live ? ca : -1;
+                    float term = live ? cm : 0.0f;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) term += __shfl_xor_sync(0xffffffffu, term, off);
-                if (lane == 0) sh->gsum[par][g] = term;
+                    for (int off = 16; off > 0; off >>= 1) term += __shfl_xor_sync(0xffffffffu, term, off);
+                    total += term;
+                }
+                // the partials of this group are read before the next group's overwrite them
+                ptx::mbar_arrive(ptx::smem_u32(&bars->red_mid));
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->red_mid), mph, err);
+                ok = __all_sync(0xffffffffu, ok);
+                mph ^= 1;
+                if (!ok) break;
             }
-            // combine the groups' sums in group order
-            ptx::mbar_arrive(ptx::smem_u32(&bars->grp_sum[par]));
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->grp_sum[par]), gph[par], err);
-            ok = __all_sync(0xffffffffu, ok);
-            gph[par] ^= 1;
             if (!ok) break;
-            if (g == 0 && quarter == 0 && lane == 0) {
-                float total = 0.0f;
-                for (int gg = 0; gg < p.groups; ++gg) total += sh->gsum[par][gg];
-                p.scores[pair] = rec.nonempty ? total : kEmptyDocScore;
-            }
-            par ^= 1;
+            if (quarter == 0 && lane == 0) p.scores[pair] = info.nonempty ? total : kEmptyDocScore;
+            ptx::mbar_arrive(ptx::smem_u32(&bars->dump_empty[db]));
+            if (++db == 2) { db = 0; dph ^= 1; }
         }
     }
 
@@ -515,7 +554,7 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
     p.acc_cols = cols;
     p.q_bytes = static_cast<uint32_t>(p.atoms * p.np * kAtomBytes);
     p.d_bytes = static_cast<uint32_t>(p.atoms * kRows * kAtomBytes);
-    const size_t misc = sizeof(Bars) + sizeof(Shared);
+    const size_t misc = sizeof(Bars) + sizeof(Shared) + 2 * static_cast<size_t>(p.groups) * sizeof(Dump);
     const size_t budget = static_cast<size_t>(info.max_smem_optin) - 1024 - misc - 2 * p.q_bytes;
     p.stages = static_cast<int>(budget / p.d_bytes);
     if (p.stages > kMaxStages) p.stages = kMaxStages;
@@ -546,7 +585,7 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = P.n_pairs < info.sm_count ? P.n_pairs : info.sm_count;
-    const int threads = 32 * (2 + 4 * p.groups);
+    const int threads = 32 * (2 + 4 * p.groups + 4);
     stream_fwd_tc_kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(tmq, tmd, p);
     return cudaGetLastError();
 }

@@ -75,7 +75,7 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
                                    cudaStream_t stream);
 
 // Tensor-core (tcgen05) streaming forward for the pairwise and kd layouts,
-// fp16/bf16: dim % 16 == 0, dim <= 256, 1 <= Lq <= 64, Ld >= 1.
+// fp16/bf16: dim % 16 == 0, dim <= 256, 1 <= Lq <= 32, Ld >= 1.
 bool tc_stream_eligible(const Problem& P);
 cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax,
                                  cudaStream_t stream);

@@ -81,6 +81,8 @@ SWEEP = [
     ("pairwise",   7,  0, 32,  700,  128),
     ("pairwise",   4,  0, 20, 2100,  128),
     ("pairwise",   3,  0, 128, 129,   64),
+    ("pairwise",   5,  0, 48,  300,  128),
+    ("kd",         3,  4, 33,  200,   64),
     ("kd",         3,  5, 32,  260,  128),
     ("kd",         2, 17, 32, 1030,  128),
     ("kd",         4,  3, 16,   77,   32),
