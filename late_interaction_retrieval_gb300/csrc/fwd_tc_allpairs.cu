@@ -109,19 +109,17 @@ __device__ __forceinline__ float max16(const float (&v)[16]) {
     return max3f(max3f(a, b, c), fmaxf(d, e), v[15]);
 }
 
-// 16 consecutive accumulator columns of this thread's row.  `mw` holds the
-// 16 column-validity bits.  Returns the exact max over the valid columns
-// and, when kArg, the column of a maximum: the lowest column whose value
-// equals the max in every bit but the last four.  That index comes from a
-// second max over packed keys (value with its low 4 mantissa bits replaced
-// by 15 - column), so each column costs one LOP3 and a third of two 3-input
-// maxima instead of a compare and two selects.  A column picked this way
-// holds the max or a value within 2^-19 of it relative; exact ties between
-// non-negative values resolve to the lowest column.
+// 16 consecutive accumulator columns of this thread's row, already loaded.
+// `mw` holds the 16 column-validity bits.  Returns the exact max over the
+// valid columns and, when kArg, the column of a maximum: the lowest column
+// whose value equals the max in every bit but the last four.  That index
+// comes from a second max over packed keys (value with its low 4 mantissa
+// bits replaced by 15 - column), so each column costs one LOP3 and a third
+// of two 3-input maxima instead of a compare and two selects.  A column
+// picked this way holds the max or a value within 2^-19 of it relative;
+// exact ties between non-negative values resolve to the lowest column.
 template <bool kArg>
-__device__ __forceinline__ void chunk_best16(uint32_t taddr, uint32_t mw, float& best, int& idx) {
-    uint32_t raw[16];
-    ptx::tmem_ld_16(taddr, raw);
+__device__ __forceinline__ void unit_best16(uint32_t (&raw)[16], uint32_t mw, float& best, int& idx) {
     if (mw != 0xffffu) {
 #pragma unroll
         for (int t = 0; t < 16; ++t) raw[t] = ((mw >> t) & 1u) ? raw[t] : 0xff7fffffu;  // -FLT_MAX
@@ -367,17 +365,26 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::tc_fence_after();
             const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
             const int jt = cur.t * p.T;
+            // units wg + 4k, two per TMEM round trip (columns past T read harmless
+            // values of the 256-column buffer and are masked out)
 #pragma unroll
-            for (int k = 0; k < kUnitsPerGroup; ++k) {
-                const int unit = wg + kEpiGroups * k;
-                const uint32_t hw = (mw[k >> 1] >> (16 * (k & 1))) & 0xffffu;
-                if (hw == 0) continue;  // no valid column (or past the tile)
-                float cb;
-                int ci;
-                chunk_best16<kArg>(acc + unit * 16, hw, cb, ci);
-                if (cb > m) {
-                    m = cb;
-                    am = jt + unit * 16 + ci;
+            for (int k2 = 0; k2 < kUnitsPerGroup; k2 += 2) {
+                const uint32_t w2 = mw[k2 >> 1];
+                if (w2 == 0) continue;
+                const int u0 = wg + kEpiGroups * k2, u1 = u0 + kEpiGroups;
+                uint32_t ra[16], rb[16];
+                ptx::tmem_ld_16x2(acc + u0 * 16, acc + u1 * 16, ra, rb);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t hw = (w2 >> (16 * h)) & 0xffffu;
+                    if (hw == 0) continue;
+                    float cb;
+                    int ci;
+                    unit_best16<kArg>(h == 0 ? ra : rb, hw, cb, ci);
+                    if (cb > m) {
+                        m = cb;
+                        am = jt + (h == 0 ? u0 : u1) * 16 + ci;
+                    }
                 }
             }
             ptx::tc_fence_before();

@@ -23,8 +23,9 @@
 // token and each column one query token.
 //
 // Roles (one CTA per SM, persistent over a contiguous range of pairs):
-//   warp 0      producer.  All 32 lanes read the document mask a tile ahead
-//               and build the tile's 128-bit row-validity mask; tiles with no
+//   warp 0      producer.  All 32 lanes read the document mask a window of
+//               8 tiles ahead and build each tile's 128-bit row-validity mask
+//               (one ballot per 32 rows); tiles with no
 //               valid token are skipped (never loaded).  Lane 0 issues the
 //               TMA loads (a query's rows into one of two buffers when the
 //               query changes, document tiles per stage) and publishes,
@@ -59,6 +60,7 @@ constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 8;
 constexpr int kAccBufs = 4;
 constexpr int kRing = 16;           // tile records in flight
+constexpr int kWin = 8;             // tiles whose mask bytes the producer loads together
 constexpr int kMaxGroups = 1;       // Lq <= 32 (the double-buffered dump fits shared memory)
 
 enum : int { kRecTile = 0, kRecDocEnd = 1, kRecStop = 2 };
@@ -118,6 +120,7 @@ struct DumpInfo {
 };
 
 struct Shared {
+    uint32_t win[kWin][4];   // producer: row-validity words of the current window
     Rec rec[kRing];
     StageMeta meta[kMaxStages];
     DumpInfo info[2];
@@ -251,66 +254,93 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         };
 
         const int64_t tiles = (p.Ld + kRows - 1) / kRows;
-        // the mask bytes of the next (pair, tile) are loaded one step ahead
-        uint8_t mb[4] = {0, 0, 0, 0};
-        if (pb < pe) load_tile_mask(p, doc_of(p, pb), 0, lane, mb);
+        const int64_t total = (pe - pb) * tiles;  // flat (pair, tile) positions of this CTA
+        // Document-mask bytes are read a window of kWin tiles ahead (4 bytes
+        // per lane per tile, all loads in flight together), so the producer
+        // never waits on a mask load while the stream needs tiles.
+        uint8_t wb[kWin][4];
+        int64_t lp = pb, lt = 0;  // position the next window load starts at
+        auto load_window = [&]() {
+#pragma unroll
+            for (int k = 0; k < kWin; ++k) {
+                if (lp < pe) {
+                    load_tile_mask(p, doc_of(p, lp), lt * kRows, lane, wb[k]);
+                    if (++lt == tiles) { lt = 0; ++lp; }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) wb[k][j] = 0;
+                }
+            }
+        };
+        load_window();
+        int64_t cp = pb, ct = 0;  // position being published
         int64_t q_loaded = -1;
         int qb_cur = 0;
-        for (int64_t cp = pb; ok && cp < pe; ++cp) {
-            const int64_t d = doc_of(p, cp);
-            bool any_tile = false;
-            for (int64_t ct = 0; ok && ct < tiles; ++ct) {
+        bool any_tile = false;
+        for (int64_t g0 = 0; ok && g0 < total; g0 += kWin) {
+            // validity words of this window, then the next window's loads
+#pragma unroll
+            for (int k = 0; k < kWin; ++k)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t w = __ballot_sync(0xffffffffu, wb[k][j] != 0);
+                    if (lane == 0) sh->win[k][j] = w;
+                }
+            __syncwarp();
+            load_window();
+            for (int k = 0; ok && k < kWin && g0 + k < total; ++k) {
+                const int64_t d = doc_of(p, cp);
+                if (ct == 0) any_tile = false;
                 uint32_t w[4];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) w[k] = __ballot_sync(0xffffffffu, mb[k] != 0);
-                {
-                    int64_t np_ = cp, nt = ct + 1;
-                    if (nt == tiles) { np_ = cp + 1; nt = 0; }
-                    if (np_ < pe) load_tile_mask(p, doc_of(p, np_), nt * kRows, lane, mb);
-                }
-                if ((w[0] | w[1] | w[2] | w[3]) == 0) continue;  // no valid token: never loaded
-                StageMeta meta{};
-                if (!any_tile) {
-                    any_tile = true;
-                    const int64_t q = query_of(p, cp);
-                    if (q != q_loaded) {
-                        // the query's rows, into the buffer the MMA released when it
-                        // started the query before the previous one
-                        if (lane == 0) {
-                            ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_q[qb]), qph ^ 1, err);
-                            if (ok) {
-                                const uint32_t fq = ptx::smem_u32(&bars->full_q[qb]);
-                                ptx::mbar_arrive_expect_tx(fq, p.q_bytes);
-                                for (int a = 0; a < p.atoms; ++a)
-                                    ptx::tma_load_2d(ptx::smem_u32(qbuf + qb * p.q_bytes + a * p.np * kAtomBytes),
-                                                     &tmq, a * kAtomElems, static_cast<int32_t>(q * p.Lq), fq);
-                                issued_q |= 1u << qb;
-                                last_ph_q = (last_ph_q & ~(1u << qb)) | (qph << qb);
+                for (int j = 0; j < 4; ++j) w[j] = sh->win[k][j];
+                if ((w[0] | w[1] | w[2] | w[3]) != 0) {
+                    StageMeta meta{};
+                    if (!any_tile) {
+                        any_tile = true;
+                        const int64_t q = query_of(p, cp);
+                        if (q != q_loaded) {
+                            // the query's rows, into the buffer the MMA released when it
+                            // started the query before the previous one
+                            if (lane == 0) {
+                                ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_q[qb]), qph ^ 1, err);
+                                if (ok) {
+                                    const uint32_t fq = ptx::smem_u32(&bars->full_q[qb]);
+                                    ptx::mbar_arrive_expect_tx(fq, p.q_bytes);
+                                    for (int a = 0; a < p.atoms; ++a)
+                                        ptx::tma_load_2d(ptx::smem_u32(qbuf + qb * p.q_bytes + a * p.np * kAtomBytes),
+                                                         &tmq, a * kAtomElems, static_cast<int32_t>(q * p.Lq), fq);
+                                    issued_q |= 1u << qb;
+                                    last_ph_q = (last_ph_q & ~(1u << qb)) | (qph << qb);
+                                }
                             }
+                            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                            if (!ok) break;
+                            q_loaded = q;
+                            qb_cur = qb;
+                            if (++qb == 2) { qb = 0; qph ^= 1; }
+                            meta.new_query = 1;
                         }
-                        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                        if (!ok) break;
-                        q_loaded = q;
-                        qb_cur = qb;
-                        if (++qb == 2) { qb = 0; qph ^= 1; }
-                        meta.new_query = 1;
                     }
-                }
-                meta.qb = qb_cur;
-                Rec rec{};
-                rec.kind = kRecTile;
-                rec.jt = static_cast<int>(ct * kRows);
+                    meta.qb = qb_cur;
+                    Rec rec{};
+                    rec.kind = kRecTile;
+                    rec.jt = static_cast<int>(ct * kRows);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) rec.valid[k] = w[k];
-                if (!(ok = publish(rec))) break;
-                if (!(ok = stage(meta, true, d, ct * kRows))) break;
+                    for (int j = 0; j < 4; ++j) rec.valid[j] = w[j];
+                    if (!(ok = publish(rec))) break;
+                    if (!(ok = stage(meta, true, d, ct * kRows))) break;
+                }
+                if (ct == tiles - 1) {
+                    Rec end{};
+                    end.kind = kRecDocEnd;
+                    end.pair = cp;
+                    end.nonempty = any_tile ? 1 : 0;
+                    if (!(ok = publish(end))) break;
+                }
+                if (++ct == tiles) { ct = 0; ++cp; }
             }
-            if (!ok) break;
-            Rec end{};
-            end.kind = kRecDocEnd;
-            end.pair = cp;
-            end.nonempty = any_tile ? 1 : 0;
-            if (!(ok = publish(end))) break;
+            __syncwarp();  // the window's words are read before the next window overwrites them
         }
         if (ok) {
             StageMeta stop{};
