@@ -26,8 +26,9 @@
 //               warpgroups split each tile's 16-column units round-robin
 //               (unit u goes to group u % 4), keep a running (max, argmax)
 //               per row, and merge at the end of every document.
-// The accumulator is double-buffered in TMEM (2 x 256 columns), so the MMA of
-// tile t+1 overlaps the epilogue of tile t.
+// The accumulator is multi-buffered in TMEM (512 columns split into 2..4
+// buffers, as many as the tile width allows), so the MMA runs ahead of the
+// epilogue.
 //
 // Epilogue per 16-column unit: the document mask as warp-uniform bits (one
 // ballot per two units, loaded a tile ahead), one tcgen05.ld, an exact max
@@ -57,11 +58,14 @@ constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 6;
-constexpr int kAccCols = 256;        // TMEM columns per accumulator buffer
+constexpr int kMaxTileCols = 256;     // widest document tile (MMA N)
+constexpr int kTmemCols = 512;        // all of TMEM; split into p.nacc accumulator buffers
+constexpr int kMaxAcc = 4;
 
 struct Params {
     int64_t Nq, Nd, Lq, Ld;
     int dim, atoms, T, tiles_per_doc, qpt, n_rb, dpu, stages;
+    int nacc, acc_stride;  // accumulator buffers in TMEM and their column stride
     int64_t n_units;
     uint32_t idesc, q_bytes, d_bytes;
     const uint8_t* qmask;
@@ -75,7 +79,7 @@ struct Params {
 struct Bars {
     uint64_t full_d[kMaxStages], empty_d[kMaxStages];
     uint64_t full_q[2], empty_q[2];
-    uint64_t acc_full[2], acc_empty[2];
+    uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc];
     uint64_t xfull;     // warpgroups 1..3 have published a document's (max, argmax)
     uint64_t xfree;     // warpgroup 0 has read them
     uint64_t qsum[2];   // per-query sums inside warpgroup 0 (128)
@@ -204,9 +208,11 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->qsum[b]), 128);
+        }
+        for (int b = 0; b < kMaxAcc; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), kEpiWarps);
-            ptx::mbar_init(ptx::smem_u32(&bars->qsum[b]), 128);
         }
         ptx::mbar_init(ptx::smem_u32(&bars->xfull), (kEpiWarps - 4) * 32);
         ptx::mbar_init(ptx::smem_u32(&bars->xfree), 4 * 32);
@@ -214,7 +220,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
-        ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), 2 * kAccCols);
+        ptx::tmem_alloc(ptx::smem_u32(&bars->tmem_base), kTmemCols);
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
@@ -288,7 +294,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                         if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[ab]), aph ^ 1, err))) break;
                         ptx::tc_fence_after();
                         const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
-                        const uint32_t acc = tmem_base + ab * kAccCols;
+                        const uint32_t acc = tmem_base + ab * p.acc_stride;
                         bool accumulate = false;
                         for (int a = 0; a < p.atoms; ++a) {
                             const int ks = ksteps_of_atom(p.dim, a);
@@ -302,7 +308,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                         ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
                         ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
                         if (++s == p.stages) { s = 0; ph ^= 1; }
-                        if (++ab == 2) { ab = 0; aph ^= 1; }
+                        if (++ab == p.nacc) { ab = 0; aph ^= 1; }
                     }
                 }
                 ptx::mma_commit(ptx::smem_u32(&bars->empty_q[qb]));
@@ -363,17 +369,24 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            const uint32_t acc = tmem_base + ab * kAccCols + lane_off;
+            const uint32_t acc = tmem_base + ab * p.acc_stride + lane_off;
             const int jt = cur.t * p.T;
-            // units wg + 4k, two per TMEM round trip (columns past T read harmless
-            // values of the 256-column buffer and are masked out)
+            // units wg + 4k, two per TMEM round trip; a unit past the tile width is
+            // never read (its columns may lie past this buffer, or past TMEM)
 #pragma unroll
             for (int k2 = 0; k2 < kUnitsPerGroup; k2 += 2) {
                 const uint32_t w2 = mw[k2 >> 1];
                 if (w2 == 0) continue;
                 const int u0 = wg + kEpiGroups * k2, u1 = u0 + kEpiGroups;
                 uint32_t ra[16], rb[16];
-                ptx::tmem_ld_16x2(acc + u0 * 16, acc + u1 * 16, ra, rb);
+                if (u1 * 16 < p.T) {
+                    ptx::tmem_ld_16x2(acc + u0 * 16, acc + u1 * 16, ra, rb);
+                } else {
+                    // w2 != 0 implies u0 lies inside the tile
+                    ptx::tmem_ld_16(acc + u0 * 16, ra);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) rb[t] = 0;
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t hw = (w2 >> (16 * h)) & 0xffffu;
@@ -390,7 +403,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[ab]));
-            if (++ab == 2) { ab = 0; aph ^= 1; }
+            if (++ab == p.nacc) { ab = 0; aph ^= 1; }
 
             if (cur.t == p.tiles_per_doc - 1) {
                 // ---- document end: merge the warpgroups' (max, argmax).
@@ -476,7 +489,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem_base, 2 * kAccCols);
+        ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -503,9 +516,14 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
     p.Ld = P.Ld;
     p.dim = static_cast<int>(P.dim);
     p.atoms = (p.dim + kAtomElems - 1) / kAtomElems;
-    const int tmax = p.atoms <= 2 ? 256 : 128;
+    const int tmax = p.atoms <= 2 ? kMaxTileCols : 128;
     p.tiles_per_doc = ceil_div(P.Ld, tmax);
     p.T = ((ceil_div(P.Ld, p.tiles_per_doc) + 15) / 16) * 16;
+    // as many accumulator buffers as TMEM holds at a 32-column-aligned stride
+    p.acc_stride = ((p.T + 31) / 32) * 32;
+    p.nacc = kTmemCols / p.acc_stride;
+    if (p.nacc > kMaxAcc) p.nacc = kMaxAcc;
+    p.acc_stride = (kTmemCols / p.nacc) / 32 * 32;
     p.qpt = static_cast<int>(kM / P.Lq);
     p.n_rb = ceil_div(P.n_query, p.qpt);
     p.q_bytes = static_cast<uint32_t>(p.atoms * kM * kAtomBytes);

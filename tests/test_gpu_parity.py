@@ -78,6 +78,8 @@ SWEEP = [
     ("allpairs",   3,  6, 100,  33,  256),
     ("allpairs",   2,  2,  7,   31,   16),
     ("allpairs",   2,  3,  5,   40,   96),
+    ("allpairs",   4, 400, 32, 300,  128),  # 160-column tiles, 3 accumulators, several per CTA
+    ("allpairs",   1, 700, 128, 140, 128),  # 144-column tiles, many per CTA
     ("pairwise",   7,  0, 32,  700,  128),
     ("pairwise",   4,  0, 20, 2100,  128),
     ("pairwise",   3,  0, 128, 129,   64),
