@@ -26,19 +26,19 @@ constexpr int kWarps = kThreads / 32;
 
 // ------------------------------------------------------------- grad_Q --
 //
-// Vector path (dim % 8 == 0, dim <= 256): one CTA per (query, group of 32
-// query tokens), 2 x 256 threads.  Eight threads own one token row, each a
-// set of 8-element vectors (16 B of fp16/bf16); the two 256-thread halves
+// Vector path (dim % 8 == 0, dim <= 256): one CTA per (query, group of 16
+// query tokens), 2 x 128 threads.  Eight threads own one token row, each a
+// set of 8-element vectors (16 B of fp16/bf16); the two 128-thread halves
 // take alternate pairs of the query.  The pairs are visited in chunks whose
 // argmax slice and upstream gradients (both contiguous in memory) are staged
 // in shared memory; every thread then gathers its document rows with
 // independent 16-byte loads, eight pairs at a time.  The halves' partial sums
 // are added in a fixed order at the end, so the result is deterministic.
 
-constexpr int kRowsPerCta = 32;
+constexpr int kRowsPerCta = 16;
 constexpr int kThreadsPerRow = 8;
 constexpr int kPairGroups = 2;
-constexpr int kVecThreads = kRowsPerCta * kThreadsPerRow * kPairGroups;  // 512
+constexpr int kVecThreads = kRowsPerCta * kThreadsPerRow * kPairGroups;  // 256
 constexpr int kVec = 8;                                                  // elements per vector
 constexpr int kPairChunk = 64;
 
@@ -78,7 +78,7 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
     const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t q = blockIdx.x / groups;
     const int64_t i0 = (blockIdx.x - q * groups) * kRowsPerCta;
-    const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group 0 / 1
+    const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group
     const int tl = threadIdx.x % (kRowsPerCta * kThreadsPerRow);
     const int r = tl / kThreadsPerRow, sub = tl % kThreadsPerRow;
     const int rows_here = static_cast<int>(P.Lq - i0 < kRowsPerCta ? P.Lq - i0 : kRowsPerCta);
