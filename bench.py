@@ -37,9 +37,12 @@ from late_interaction_retrieval_gb300 import workloads as W  # noqa: E402
 METRIC = "MaxSim fwd+bwd TFLOP/s (% dense bf16 peak); pairwise GB/s (% HBM peak)"
 L2_FLUSH_BYTES = 256 << 20  # > 129 MB L2
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+_CSRC = "late_interaction_retrieval_gb300/csrc/"
+# every source file a kernel's code comes from: its DRAM counters stay valid
+# only while all of them are unchanged
 KERNEL_SOURCES = {
-    "allpairs_fwd_tc_kernel": "late_interaction_retrieval_gb300/csrc/fwd_tc_allpairs.cu",
-    "stream_fwd_tc_kernel": "late_interaction_retrieval_gb300/csrc/fwd_tc_stream.cu",
+    "allpairs_fwd_tc_kernel": (_CSRC + "fwd_tc_allpairs.cu", _CSRC + "sm100_ptx.cuh", _CSRC + "lik_internal.h"),
+    "stream_fwd_tc_kernel": (_CSRC + "fwd_tc_stream.cu", _CSRC + "sm100_ptx.cuh", _CSRC + "lik_internal.h"),
 }
 
 
@@ -89,11 +92,18 @@ def kernel_traffic(kernel: str, workload: str):
     ent = table.get(kernel, {}).get(workload)
     if not ent:
         return None
-    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    if ent.get("source_sha256") != sha:
+    if ent.get("source_sha256") != source_digest(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def source_digest(kernel: str) -> str:
+    """sha256 over the kernel's source files, in the listed order."""
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:

@@ -56,6 +56,7 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kUnitsPerGroup = 4;      // 16-column units per tile per warpgroup (T <= 256)
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
+constexpr int kMaxDim = 256;        // largest embedding size the tensor-core paths take
 constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 6;
 constexpr int kMaxTileCols = 256;     // widest document tile (MMA N)
@@ -94,11 +95,6 @@ struct Exchange {
     uint32_t any[kEpiGroups - 1][4];
     float part[2][kM];               // per-row terms or per-warp partial sums (warpgroup 0)
 };
-
-__device__ __forceinline__ int ksteps_of_atom(int dim, int a) {
-    const int rem = dim - a * kAtomElems;
-    return (rem >= kAtomElems ? kAtomElems : rem) / 16;
-}
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;
@@ -295,16 +291,11 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                         ptx::tc_fence_after();
                         const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
                         const uint32_t acc = tmem_base + ab * p.acc_stride;
-                        bool accumulate = false;
-                        for (int a = 0; a < p.atoms; ++a) {
-                            const int ks = ksteps_of_atom(p.dim, a);
-                            for (int kk = 0; kk < ks; ++kk) {
-                                const uint64_t ad = ptx::sw128_kmajor_desc(qaddr + a * kM * kAtomBytes + kk * 32);
-                                const uint64_t bd = ptx::sw128_kmajor_desc(daddr + a * p.T * kAtomBytes + kk * 32);
-                                ptx::mma_f16(acc, ad, bd, p.idesc, accumulate);
-                                accumulate = true;
-                            }
-                        }
+                        if (p.dim == 128)  // the common embedding size: no per-step guards
+                            ptx::mma_kchain<8>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes, 8, p.idesc);
+                        else
+                            ptx::mma_kchain<kMaxDim / 16>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes,
+                                                          p.dim / 16, p.idesc);
                         ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
                         ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
                         if (++s == p.stages) { s = 0; ph ^= 1; }
@@ -499,7 +490,7 @@ int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
 bool tc_allpairs_eligible(const Problem& P) {
     return P.layout == kAllPairs && (P.dtype == kF16 || P.dtype == kBF16) && P.dim % 16 == 0 &&
-           P.dim <= 256 && P.Lq >= 1 && P.Lq <= kM && P.Ld >= 1 && P.n_query * P.Lq < (int64_t(1) << 31) &&
+           P.dim <= kMaxDim && P.Lq >= 1 && P.Lq <= kM && P.Ld >= 1 && P.n_query * P.Lq < (int64_t(1) << 31) &&
            P.Ld < (int64_t(1) << 31) && P.n_doc < (int64_t(1) << 31);
 }
 

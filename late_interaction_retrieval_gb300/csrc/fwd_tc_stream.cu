@@ -56,6 +56,7 @@ namespace {
 
 constexpr int kRows = 128;          // document tokens per tile (MMA M)
 constexpr int kAtomBytes = 128;     // one 128-byte swizzle row = 64 fp16/bf16
+constexpr int kMaxDim = 256;       // largest embedding size the tensor-core paths take
 constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 8;
 constexpr int kAccBufs = 4;
@@ -135,11 +136,6 @@ __device__ __forceinline__ int64_t doc_of(const Params& p, int64_t pair) {
 
 __device__ __forceinline__ int64_t query_of(const Params& p, int64_t pair) {
     return pair / p.pairs_per_query;
-}
-
-__device__ __forceinline__ int ksteps_of_atom(int dim, int a) {
-    const int rem = dim - a * kAtomElems;
-    return (rem >= kAtomElems ? kAtomElems : rem) / 16;
 }
 
 // Mask bytes of the tile starting at token jt of document d: lane l holds
@@ -382,16 +378,11 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
                 const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
                 const uint32_t qaddr = ptx::smem_u32(qbuf + meta.qb * p.q_bytes);
                 const uint32_t acc = tmem_base + ab * p.np;
-                bool accumulate = false;
-                for (int a = 0; a < p.atoms; ++a) {
-                    const int ks = ksteps_of_atom(p.dim, a);
-                    for (int kk = 0; kk < ks; ++kk) {
-                        const uint64_t ad = ptx::sw128_kmajor_desc(daddr + a * kRows * kAtomBytes + kk * 32);
-                        const uint64_t bd = ptx::sw128_kmajor_desc(qaddr + a * p.np * kAtomBytes + kk * 32);
-                        ptx::mma_f16(acc, ad, bd, p.idesc, accumulate);
-                        accumulate = true;
-                    }
-                }
+                if (p.dim == 128)  // the common embedding size: no per-step guards
+                    ptx::mma_kchain<8>(acc, daddr, kRows * kAtomBytes, qaddr, p.np * kAtomBytes, 8, p.idesc);
+                else
+                    ptx::mma_kchain<kMaxDim / 16>(acc, daddr, kRows * kAtomBytes, qaddr, p.np * kAtomBytes,
+                                                  p.dim / 16, p.idesc);
                 ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
                 ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
                 if (++s == p.stages) { s = 0; ph ^= 1; }
@@ -557,7 +548,7 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 
 bool tc_stream_eligible(const Problem& P) {
     return (P.layout == kPairwise || P.layout == kKd) && (P.dtype == kF16 || P.dtype == kBF16) &&
-           P.dim % 16 == 0 && P.dim <= 256 && P.Lq >= 1 && P.Lq <= 32 * kMaxGroups && P.Ld >= 1 &&
+           P.dim % 16 == 0 && P.dim <= kMaxDim && P.Lq >= 1 && P.Lq <= 32 * kMaxGroups && P.Ld >= 1 &&
            P.n_query * P.Lq < (int64_t(1) << 31) && P.Ld < (int64_t(1) << 31) &&
            P.n_doc < (int64_t(1) << 31);
 }

@@ -164,6 +164,28 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t addr) {
     return d;
 }
 
+// One accumulator tile D = A . B^T over K = 16 * nk, issued as nk
+// tcgen05.mma of K = 16.  A and B are SW128 K-major tiles split into atoms
+// of 64 elements (128 B) along K; atom `a` of A starts at a_base + a * a_atom
+// bytes (b likewise), and k-step k reads atom k / 4 at byte offset
+// 32 * (k % 4).  The first step overwrites D, the rest accumulate.
+// The chain is unrolled to kMaxK guarded steps (none left when nk is a
+// compile-time kMaxK): the same instructions under a runtime-bounded loop
+// ran about 1.5x slower on sm_103a (measured on a loop of MMAs alone).
+template <int kMaxK>
+__device__ __forceinline__ void mma_kchain(uint32_t d_tmem, uint32_t a_base, uint32_t a_atom, uint32_t b_base,
+                                           uint32_t b_atom, int nk, uint32_t idesc) {
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < nk) {
+            const uint32_t off = static_cast<uint32_t>(k & 3) * 32;
+            const uint32_t atom = static_cast<uint32_t>(k >> 2);
+            mma_f16(d_tmem, sw128_kmajor_desc(a_base + atom * a_atom + off),
+                    sw128_kmajor_desc(b_base + atom * b_atom + off), idesc, k != 0);
+        }
+    }
+}
+
 // Instruction descriptor of tcgen05.mma .kind::f16: fp32 accumulator,
 // A and B of one type (bf16 when `bf16`, else fp16), both K-major, M x N.
 __host__ __device__ constexpr uint32_t f16_idesc(int M, int N, bool bf16) {
