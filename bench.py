@@ -230,12 +230,15 @@ class Step:
         return int(2 * w.dim * tot)
 
     def algorithmic_bytes(self) -> int:
-        """Bytes a forward must move at least: valid D rows, Q, masks, scores."""
+        """Bytes a forward must move at least: valid D rows, Q, masks, scores,
+        and the saved argmax when the step keeps one for its backward."""
         i, w = self.inp, self.w
         el = i.Q.element_size()
         dv = int(i.dmask.sum())
         qbytes = i.Q.numel() * el
-        return dv * w.dim * el + i.dmask.numel() + qbytes + i.qmask.numel() + self.scores.numel() * 4
+        saved = self.argmax.numel() * 4 if self.argmax is not None else 0
+        return (dv * w.dim * el + i.dmask.numel() + qbytes + i.qmask.numel() + self.scores.numel() * 4
+                + saved)
 
 
 # ---------------------------------------------------------------- our arm --

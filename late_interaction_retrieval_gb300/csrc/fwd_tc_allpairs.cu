@@ -31,12 +31,16 @@
 // epilogue.
 //
 // Epilogue per 16-column unit: the document mask as warp-uniform bits (one
-// ballot per two units, loaded a tile ahead), one tcgen05.ld, an exact max
-// by 3-input max instructions and the column of the max by a packed-key max
-// (chunk_best16), and a strictly-greater merge into the running max, so
-// exact ties between units go to the lowest token index, as in the oracle.  At a document's end the
-// maxima of the valid query tokens are summed per query (fixed order) and
-// the score and argmax are written.
+// ballot per two units, loaded a tile ahead) and one tcgen05.ld.red, which
+// returns the unit's 16 values together with their maximum (an sm_103a
+// load-with-reduction), so a fully valid unit costs no ALU work for its max.
+// A unit with masked columns takes its max over the valid ones instead.
+// When argmax is wanted, a unit whose max is strictly larger than the row's
+// running max keeps its 16 values in registers; at the document's end the
+// lowest column equal to the max is picked from them.  Exact ties therefore
+// go to the lowest token index, as in the oracle.  The maxima of the valid
+// query tokens are then summed per query (fixed order) and the score and
+// argmax written.
 //
 // Every mbarrier wait is bounded (ptx::mbar_wait); on expiry the kernel sets
 // the library's error word, drains its own TMA loads and MMAs, frees TMEM and
@@ -53,13 +57,14 @@ namespace {
 constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kUnitsPerGroup = 4;      // 16-column units per tile per warpgroup (T <= 256)
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kMaxDim = 256;        // largest embedding size the tensor-core paths take
 constexpr int kAtomElems = 64;
 constexpr int kMaxStages = 6;
 constexpr int kMaxTileCols = 256;     // widest document tile (MMA N)
+// 16-column units of a tile per warpgroup, rounded up to pairs (one TMEM round trip each)
+constexpr int kUnitsPerGroup = 2 * ((kMaxTileCols / 16 + 2 * kEpiGroups - 1) / (2 * kEpiGroups));
 constexpr int kTmemCols = 512;        // all of TMEM; split into p.nacc accumulator buffers
 constexpr int kMaxAcc = 4;
 
@@ -109,33 +114,47 @@ __device__ __forceinline__ float max16(const float (&v)[16]) {
     return max3f(max3f(a, b, c), fmaxf(d, e), v[15]);
 }
 
-// 16 consecutive accumulator columns of this thread's row, already loaded.
-// `mw` holds the 16 column-validity bits.  Returns the exact max over the
-// valid columns and, when kArg, the column of a maximum: the lowest column
-// whose value equals the max in every bit but the last four.  That index
-// comes from a second max over packed keys (value with its low 4 mantissa
-// bits replaced by 15 - column), so each column costs one LOP3 and a third
-// of two 3-input maxima instead of a compare and two selects.  A column
-// picked this way holds the max or a value within 2^-19 of it relative;
-// exact ties between non-negative values resolve to the lowest column.
-template <bool kArg>
-__device__ __forceinline__ void unit_best16(uint32_t (&raw)[16], uint32_t mw, float& best, int& idx) {
-    if (mw != 0xffffu) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) raw[t] = ((mw >> t) & 1u) ? raw[t] : 0xff7fffffu;  // -FLT_MAX
-    }
+// Max over the valid columns of a 16-column unit whose validity bits `mw`
+// are not all set; invalid columns are overwritten with -FLT_MAX in `raw`,
+// so that the saved values of a unit never hold a masked maximum.
+__device__ __forceinline__ float masked_max16(uint32_t (&raw)[16], uint32_t mw) {
     float v[16];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(raw[t]);
-    best = max16(v);
-    if constexpr (kArg) {
-        float k[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) k[t] = __uint_as_float((raw[t] & 0xfffffff0u) | (15u - t));
-        idx = 15 - static_cast<int>(__float_as_uint(max16(k)) & 15u);
-    } else {
-        idx = 0;
+    for (int t = 0; t < 16; ++t) {
+        raw[t] = ((mw >> t) & 1u) ? raw[t] : 0xff7fffffu;  // -FLT_MAX
+        v[t] = __uint_as_float(raw[t]);
     }
+    return max16(v);
+}
+
+// Folds one loaded 16-column unit (validity bits `mw`, load max `mred`,
+// first column `col`) into the row's running max `m`.  With kArg a strictly
+// larger unit max also keeps the unit's values and first column; the column
+// of the max is resolved once, at the document's end.
+template <bool kArg>
+__device__ __forceinline__ void fold_unit(uint32_t (&raw)[16], uint32_t mw, float mred, int col, float& m,
+                                          int& bcol, uint32_t (&best)[16]) {
+    if (mw == 0) return;
+    // the load's own max, unless some of the unit's columns are masked
+    const float cb = mw == 0xffffu ? mred : masked_max16(raw, mw);
+    if constexpr (kArg) {
+        if (cb > m) {
+            m = cb;
+            bcol = col;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) best[t] = raw[t];
+        }
+    } else {
+        m = fmaxf(m, cb);
+    }
+}
+
+// Lowest t with v[t] == m (m is one of the 16 values).
+__device__ __forceinline__ int first_equal16(const uint32_t (&v)[16], float m) {
+    int idx = 15;
+#pragma unroll
+    for (int t = 14; t >= 0; --t) idx = (__uint_as_float(v[t]) == m) ? t : idx;
+    return idx;
 }
 
 // Position in a CTA's sequence of (work unit, document, tile).
@@ -332,8 +351,12 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         int64_t row_unit = -1;
         int64_t q = 0;
         bool row_ok = false, qvalid = false;
-        float m = -INFINITY;
-        int am = -1;
+        float m = -INFINITY;   // running max of this row over the warpgroup's units
+        int am = -1;           // its column, resolved at the document's end
+        int bcol = -1;         // first column of the unit that holds m
+        uint32_t best[16];     // that unit's values (masked columns as -FLT_MAX)
+#pragma unroll
+        for (int t = 0; t < 16; ++t) best[t] = 0;
         bool any = false;
         while (ok && cur.valid) {
             uint32_t mw[kUnitsPerGroup / 2];
@@ -350,7 +373,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             }
             if (cur.t == 0) {
                 m = -INFINITY;
-                am = -1;
+                bcol = -1;
                 any = false;
             }
 #pragma unroll
@@ -370,26 +393,18 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 if (w2 == 0) continue;
                 const int u0 = wg + kEpiGroups * k2, u1 = u0 + kEpiGroups;
                 uint32_t ra[16], rb[16];
+                float ma, mb;
                 if (u1 * 16 < p.T) {
-                    ptx::tmem_ld_16x2(acc + u0 * 16, acc + u1 * 16, ra, rb);
+                    ptx::tmem_ldmax_16x2(acc + u0 * 16, acc + u1 * 16, ra, rb, ma, mb);
                 } else {
                     // w2 != 0 implies u0 lies inside the tile
-                    ptx::tmem_ld_16(acc + u0 * 16, ra);
+                    ptx::tmem_ldmax_16(acc + u0 * 16, ra, ma);
+                    mb = -INFINITY;
 #pragma unroll
                     for (int t = 0; t < 16; ++t) rb[t] = 0;
                 }
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t hw = (w2 >> (16 * h)) & 0xffffu;
-                    if (hw == 0) continue;
-                    float cb;
-                    int ci;
-                    unit_best16<kArg>(h == 0 ? ra : rb, hw, cb, ci);
-                    if (cb > m) {
-                        m = cb;
-                        am = jt + (h == 0 ? u0 : u1) * 16 + ci;
-                    }
-                }
+                fold_unit<kArg>(ra, w2 & 0xffffu, ma, jt + u0 * 16, m, bcol, best);
+                fold_unit<kArg>(rb, w2 >> 16, mb, jt + u1 * 16, m, bcol, best);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -397,6 +412,11 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             if (++ab == p.nacc) { ab = 0; aph ^= 1; }
 
             if (cur.t == p.tiles_per_doc - 1) {
+                // the lowest column of the first unit holding this group's max
+                am = -1;
+                if constexpr (kArg) {
+                    if (bcol >= 0) am = bcol + first_equal16(best, m);
+                }
                 // ---- document end: merge the warpgroups' (max, argmax).
                 // Groups 1..3 publish (after group 0 has read the previous
                 // document's values); group 0 waits for them, then merges.

@@ -248,5 +248,37 @@ __device__ __forceinline__ void tmem_ld_16x2(uint32_t ta, uint32_t tb, uint32_t 
         : "memory");
 }
 
+// tcgen05.ld.red (sm_103a): the 16 columns as tmem_ld_16 returns them, and
+// in `mx` their maximum (IEEE max; +0 over -0), computed by the load.
+__device__ __forceinline__ void tmem_ldmax_16(uint32_t taddr, uint32_t (&v)[16], float& mx) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15}, %16, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+          "=r"(v[14]), "=r"(v[15]), "=f"(mx)
+        : "r"(taddr)
+        : "memory");
+}
+
+// Two tmem_ldmax_16 loads in flight together, one wait for both.
+__device__ __forceinline__ void tmem_ldmax_16x2(uint32_t ta, uint32_t tb, uint32_t (&a)[16], uint32_t (&b)[16],
+                                                float& ma, float& mb) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15}, %32, [%34];\n\t"
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, "
+        "%25, %26, %27, %28, %29, %30, %31}, %33, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+          "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]),
+          "=r"(a[14]), "=r"(a[15]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]),
+          "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]),
+          "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=f"(ma), "=f"(mb)
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+
 }  // namespace ptx
 }  // namespace lik
