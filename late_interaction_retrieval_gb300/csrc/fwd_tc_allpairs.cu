@@ -18,14 +18,19 @@
 //     S[128, T] = Qblock[128, dim] . Dtile[T, dim]^T      (fp32 in TMEM)
 // issued as dim/16 tcgen05.mma (kind::f16, M=128, N=T, K=16).
 //
-// Warp roles (576 threads, one CTA per SM, persistent over work units):
+// Warp roles (640 threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: Q row blocks (2 buffers) and D tiles (S stages)
 //   warp 1      TMEM allocator + single-thread MMA issuer
 //   warps 2..17 epilogue: four warpgroups; warp w reads TMEM lanes
 //               32*(w%4)..+31, i.e. one accumulator row per thread.  The
 //               warpgroups split each tile's 16-column units round-robin
-//               (unit u goes to group u % 4), keep a running (max, argmax)
-//               per row, and merge at the end of every document.
+//               (unit u goes to group u % 4) and keep a running (max, argmax)
+//               per row; at the end of a document each group hands its
+//               values to the reducers through shared memory (two slots)
+//               and goes on with the next document.
+//   warps 18,19 reducers: merge the four groups' values per row, sum each
+//               query's valid rows and write the score and argmax, while the
+//               epilogue and the MMA continue.
 // The accumulator is multi-buffered in TMEM (512 columns split into 2..4
 // buffers, as many as the tile width allows), so the MMA runs ahead of the
 // epilogue.
@@ -38,9 +43,8 @@
 // When argmax is wanted, a unit whose max is strictly larger than the row's
 // running max keeps its 16 values in registers; at the document's end the
 // lowest column equal to the max is picked from them.  Exact ties therefore
-// go to the lowest token index, as in the oracle.  The maxima of the valid
-// query tokens are then summed per query (fixed order) and the score and
-// argmax written.
+// go to the lowest token index, as in the oracle.  The reducers sum the
+// maxima of the valid query tokens per query in a fixed order.
 //
 // Every mbarrier wait is bounded (ptx::mbar_wait); on expiry the kernel sets
 // the library's error word, drains its own TMA loads and MMAs, frees TMEM and
@@ -56,7 +60,9 @@ namespace {
 
 constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kRedWarps = 2;          // document-end reducers
+constexpr int kThreads = 32 * (2 + kEpiWarps + kRedWarps);
+constexpr int kSlots = 2;             // documents in flight between the epilogue and the reducers
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kMaxDim = 256;        // largest embedding size the tensor-core paths take
@@ -86,19 +92,20 @@ struct Bars {
     uint64_t full_d[kMaxStages], empty_d[kMaxStages];
     uint64_t full_q[2], empty_q[2];
     uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc];
-    uint64_t xfull;     // warpgroups 1..3 have published a document's (max, argmax)
-    uint64_t xfree;     // warpgroup 0 has read them
-    uint64_t qsum[2];   // per-query sums inside warpgroup 0 (128)
+    uint64_t xfull[kSlots];   // every epilogue thread has published a document's (max, argmax)
+    uint64_t xfree[kSlots];   // the reducers have read them
+    uint64_t rsum[kSlots];    // the reducers' per-row terms are in shared memory
     uint64_t mma_done;
     uint32_t tmem_base;
     uint32_t pad;
 };
 
+// What the epilogue hands to the reducers at a document's end, per slot.
 struct Exchange {
-    float m[kEpiGroups - 1][kM];     // running max of warpgroups 1..3 at a document end
-    int a[kEpiGroups - 1][kM];
-    uint32_t any[kEpiGroups - 1][4];
-    float part[2][kM];               // per-row terms or per-warp partial sums (warpgroup 0)
+    float m[kSlots][kEpiGroups][kM];      // each warpgroup's max per accumulator row
+    int a[kSlots][kEpiGroups][kM];        // and its column (-1: none)
+    uint32_t any[kSlots][kEpiGroups][4];  // the warpgroup saw a valid column (per warp quarter)
+    float term[kSlots][kM];               // merged per-row terms, summed per query
 };
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -223,14 +230,16 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->qsum[b]), 128);
         }
         for (int b = 0; b < kMaxAcc; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), kEpiWarps);
         }
-        ptx::mbar_init(ptx::smem_u32(&bars->xfull), (kEpiWarps - 4) * 32);
-        ptx::mbar_init(ptx::smem_u32(&bars->xfree), 4 * 32);
+        for (int b = 0; b < kSlots; ++b) {
+            ptx::mbar_init(ptx::smem_u32(&bars->xfull[b]), kEpiWarps * 32);
+            ptx::mbar_init(ptx::smem_u32(&bars->xfree[b]), kRedWarps * 32);
+            ptx::mbar_init(ptx::smem_u32(&bars->rsum[b]), kRedWarps * 32);
+        }
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
         ptx::fence_mbar_init();
     }
@@ -328,18 +337,15 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
             ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, err);
         }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // ------------------------------------------------------ epilogue --
         const int ew = warp - 2;            // 0..kEpiWarps-1
-        const int wg = ew >> 2;             // warpgroup: chunks c with c % kEpiGroups == wg
+        const int wg = ew >> 2;             // warpgroup: units u with u % kEpiGroups == wg
         const int quarter = warp & 3;       // TMEM lane quarter of this warp
         const int r = quarter * 32 + lane;  // accumulator row of this thread
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
-        const int qloc = static_cast<int>(r / Lq);
-        const int i = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
-        int ab = 0, par = 0;
-        uint32_t aph = 0, xph = 0, sph0 = 0, sph1 = 0;
+        int ab = 0, slot = 0;
+        uint32_t aph = 0, xph = 0;
         bool ok = true;
 
         // Flat cursor over this CTA's (unit, document, tile) sequence, so the
@@ -348,11 +354,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         Cursor cur = first_cursor(p), nxt;
         uint8_t pre[kUnitsPerGroup / 2], pre_next[kUnitsPerGroup / 2];
         prefetch_mask(p, cur, wg, lane, pre);
-        int64_t row_unit = -1;
-        int64_t q = 0;
-        bool row_ok = false, qvalid = false;
         float m = -INFINITY;   // running max of this row over the warpgroup's units
-        int am = -1;           // its column, resolved at the document's end
         int bcol = -1;         // first column of the unit that holds m
         uint32_t best[16];     // that unit's values (masked columns as -FLT_MAX)
 #pragma unroll
@@ -364,13 +366,6 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             for (int k = 0; k < kUnitsPerGroup / 2; ++k) mw[k] = __ballot_sync(0xffffffffu, pre[k] != 0);
             nxt = next_cursor(p, cur);
             prefetch_mask(p, nxt, wg, lane, pre_next);
-            if (cur.u != row_unit) {
-                row_unit = cur.u;
-                const int rb = static_cast<int>(cur.u % p.n_rb);
-                q = static_cast<int64_t>(rb) * p.qpt + qloc;
-                row_ok = r < qrows && q < p.Nq;
-                qvalid = row_ok && (!p.qmask || p.qmask[q * Lq + i]);
-            }
             if (cur.t == 0) {
                 m = -INFINITY;
                 bcol = -1;
@@ -412,87 +407,108 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             if (++ab == p.nacc) { ab = 0; aph ^= 1; }
 
             if (cur.t == p.tiles_per_doc - 1) {
-                // the lowest column of the first unit holding this group's max
-                am = -1;
+                // ---- document end: hand this warpgroup's (max, argmax) of each
+                // row to the reducers and go on; the lowest column of the first
+                // unit holding the max is the group's argmax
+                int am = -1;
                 if constexpr (kArg) {
                     if (bcol >= 0) am = bcol + first_equal16(best, m);
                 }
-                // ---- document end: merge the warpgroups' (max, argmax).
-                // Groups 1..3 publish (after group 0 has read the previous
-                // document's values); group 0 waits for them, then merges.
-                if (wg > 0) {
-                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfree), xph ^ 1, err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    xph ^= 1;
-                    if (!ok) break;
-                    xc->m[wg - 1][r] = m;
-                    xc->a[wg - 1][r] = am;
-                    if (lane == 0) xc->any[wg - 1][quarter] = any ? 1u : 0u;
-                    ptx::mbar_arrive(ptx::smem_u32(&bars->xfull));
-                } else {
-                    ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull), xph, err);
-                    ok = __all_sync(0xffffffffu, ok);
-                    xph ^= 1;
-                    if (!ok) break;
-                }
-                if (wg == 0) {
-#pragma unroll
-                    for (int g2 = 0; g2 < kEpiGroups - 1; ++g2) {
-                        any = any || xc->any[g2][quarter] != 0;
-                        const float m1 = xc->m[g2][r];
-                        const int a1 = xc->a[g2][r];
-                        if (m1 > m || (m1 == m && a1 >= 0 && (am < 0 || a1 < am))) {
-                            m = m1;
-                            am = a1;
-                        }
-                    }
-                    ptx::mbar_arrive(ptx::smem_u32(&bars->xfree));
-                    const float term = (any && qvalid) ? m : 0.0f;
-                    // per-query sum over the query's rows, in a fixed order
-                    float total = 0.0f;
-                    bool writer = false;
-                    if ((Lq & 31) == 0) {
-                        float s = term;
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                        if (lane == 0) xc->part[par][quarter] = s;
-                        ptx::mbar_arrive(ptx::smem_u32(&bars->qsum[par]));
-                        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qsum[par]), par ? sph1 : sph0, err);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (par) sph1 ^= 1; else sph0 ^= 1;
-                        writer = (i == 0);
-                        if (writer) {
-                            const int w0 = r >> 5, nw = static_cast<int>(Lq >> 5);
-                            for (int w = 0; w < nw && w0 + w < 4; ++w) total += xc->part[par][w0 + w];
-                        }
-                    } else if ((32 % Lq) == 0) {
-                        float s = term;
-                        for (int off = static_cast<int>(Lq) >> 1; off > 0; off >>= 1)
-                            s += __shfl_xor_sync(0xffffffffu, s, off);
-                        writer = (i == 0);
-                        total = s;
-                    } else {
-                        xc->part[par][r] = term;
-                        ptx::mbar_arrive(ptx::smem_u32(&bars->qsum[par]));
-                        ok = ptx::mbar_wait(ptx::smem_u32(&bars->qsum[par]), par ? sph1 : sph0, err);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (par) sph1 ^= 1; else sph0 ^= 1;
-                        writer = (i == 0);
-                        if (writer)
-                            for (int64_t k = 0; k < Lq && r + k < kM; ++k) total += xc->part[par][r + k];
-                    }
-                    if (row_ok) {
-                        const int64_t pair = q * p.Nd + cur.d;
-                        if (writer) p.scores[pair] = any ? total : kEmptyDocScore;
-                        if (p.argmax) p.argmax[pair * Lq + i] = (any && qvalid) ? am : -1;
-                    }
-                }
-                par ^= 1;
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfree[slot]), xph ^ 1, err);
+                ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
+                xc->m[slot][wg][r] = m;
+                xc->a[slot][wg][r] = am;
+                if (lane == 0) xc->any[slot][wg][quarter] = any ? 1u : 0u;
+                ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[slot]));
+                if (++slot == kSlots) { slot = 0; xph ^= 1; }
             }
             cur = nxt;
 #pragma unroll
             for (int k = 0; k < kUnitsPerGroup / 2; ++k) pre[k] = pre_next[k];
+        }
+    } else {
+        // ------------------------------------------------------ reducers --
+        // Per document: merge the warpgroups' (max, argmax) per row (strictly
+        // greater wins, equal maxima keep the lower column), sum the valid
+        // query tokens' maxima per query in a fixed order, write score and
+        // argmax.  A thread owns rows rr and rr + 64.
+        constexpr int kRows = kM / (32 * kRedWarps);
+        const int rr = (warp - 2 - kEpiWarps) * 32 + lane;
+        const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
+        int slot = 0;
+        uint32_t xph = 0;
+        bool ok = true;
+        for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+            const int rb = static_cast<int>(u % p.n_rb);
+            const int64_t d0 = (u / p.n_rb) * p.dpu;
+            const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
+            int64_t q[kRows];
+            int iq[kRows];
+            bool row_ok[kRows], qvalid[kRows];
+#pragma unroll
+            for (int k = 0; k < kRows; ++k) {
+                const int r = rr + k * 32 * kRedWarps;
+                const int qloc = static_cast<int>(r / Lq);
+                iq[k] = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
+                q[k] = static_cast<int64_t>(rb) * p.qpt + qloc;
+                row_ok[k] = r < qrows && q[k] < p.Nq;
+                qvalid[k] = row_ok[k] && (!p.qmask || p.qmask[q[k] * Lq + iq[k]]);
+            }
+            for (int64_t d = d0; ok && d < d1; ++d) {
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull[slot]), xph, err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                int am[kRows];
+                bool any_doc = false;
+#pragma unroll
+                for (int k = 0; k < kRows; ++k) {
+                    const int r = rr + k * 32 * kRedWarps;
+                    float mm = xc->m[slot][0][r];
+                    int aa = xc->a[slot][0][r];
+                    bool an = xc->any[slot][0][r >> 5] != 0;
+#pragma unroll
+                    for (int g = 1; g < kEpiGroups; ++g) {
+                        const float m1 = xc->m[slot][g][r];
+                        const int a1 = xc->a[slot][g][r];
+                        an = an || xc->any[slot][g][r >> 5] != 0;
+                        if (m1 > mm || (m1 == mm && a1 >= 0 && (aa < 0 || a1 < aa))) {
+                            mm = m1;
+                            aa = a1;
+                        }
+                    }
+                    any_doc = an;  // the same for every row: validity is per column
+                    xc->term[slot][r] = (an && qvalid[k]) ? mm : 0.0f;
+                    am[k] = (an && qvalid[k]) ? aa : -1;
+                }
+                ptx::mbar_arrive(ptx::smem_u32(&bars->xfree[slot]));
+                ptx::mbar_arrive(ptx::smem_u32(&bars->rsum[slot]));
+                ok = ptx::mbar_wait(ptx::smem_u32(&bars->rsum[slot]), xph, err);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+#pragma unroll
+                for (int k = 0; k < kRows; ++k) {
+                    if (!row_ok[k]) continue;
+                    const int r = rr + k * 32 * kRedWarps;
+                    const int64_t pair = q[k] * p.Nd + d;
+                    if (iq[k] == 0) {
+                        // the query's rows r .. r + Lq - 1, four interleaved partial sums
+                        const float* t = xc->term[slot] + r;
+                        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+                        int64_t k4 = 0;
+                        for (; k4 + 4 <= Lq; k4 += 4) {
+                            s0 += t[k4];
+                            s1 += t[k4 + 1];
+                            s2 += t[k4 + 2];
+                            s3 += t[k4 + 3];
+                        }
+                        for (; k4 < Lq; ++k4) s0 += t[k4];
+                        p.scores[pair] = any_doc ? (s0 + s1) + (s2 + s3) : kEmptyDocScore;
+                    }
+                    if (p.argmax) p.argmax[pair * Lq + iq[k]] = am[k];
+                }
+                if (++slot == kSlots) { slot = 0; xph ^= 1; }
+            }
         }
     }
 
