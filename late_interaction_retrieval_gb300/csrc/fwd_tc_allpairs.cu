@@ -264,20 +264,34 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             uint32_t issued_d = 0, issued_q = 0;  // bit i: slot i holds an issued load
             uint32_t last_ph_d = 0, last_ph_q = 0;
             bool ok = true;
-            for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-                const int rb = static_cast<int>(u % p.n_rb);
-                const int64_t d0 = (u / p.n_rb) * p.dpu;
-                const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
-                if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_q[qb]), qph ^ 1, err))) break;
+            // Q row block of unit uq into the next Q buffer, once the MMAs of
+            // the unit that used it before have completed
+            auto issue_q = [&](int64_t uq) -> bool {
+                if (!ptx::mbar_wait(ptx::smem_u32(&bars->empty_q[qb]), qph ^ 1, err)) return false;
                 const uint32_t fq = ptx::smem_u32(&bars->full_q[qb]);
                 ptx::mbar_arrive_expect_tx(fq, p.q_bytes);
-                const int32_t row0 = static_cast<int32_t>(static_cast<int64_t>(rb) * p.qpt * Lq);
+                const int64_t rbq = uq % p.n_rb;
+                const int32_t row0 = static_cast<int32_t>(rbq * p.qpt * Lq);
                 for (int a = 0; a < p.atoms; ++a)
                     ptx::tma_load_2d(ptx::smem_u32(qbuf + qb * p.q_bytes + a * kM * kAtomBytes), &tmq,
                                      a * kAtomElems, row0, fq);
                 issued_q |= 1u << qb;
                 last_ph_q = (last_ph_q & ~(1u << qb)) | (qph << qb);
                 if (++qb == 2) { qb = 0; qph ^= 1; }
+                return true;
+            };
+            int64_t u = blockIdx.x;
+            if (u < p.n_units) ok = issue_q(u);
+            for (; ok && u < p.n_units; u += gridDim.x) {
+                const int64_t d0 = (u / p.n_rb) * p.dpu;
+                const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
+                // the next unit's Q goes out after this unit's first two D tiles,
+                // so its load overlaps this unit's MMAs
+                const int64_t un = u + gridDim.x;
+                bool q_next = un < p.n_units;
+                const int64_t ntiles = (d1 - d0) * p.tiles_per_doc;
+                const int64_t q_at = ntiles < 2 ? ntiles : 2;
+                int64_t k = 0;
                 for (int64_t d = d0; ok && d < d1; ++d) {
                     for (int t = 0; t < p.tiles_per_doc; ++t) {
                         if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_d[s]), ph ^ 1, err))) break;
@@ -289,6 +303,10 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                         issued_d |= 1u << s;
                         last_ph_d = (last_ph_d & ~(1u << s)) | (ph << s);
                         if (++s == p.stages) { s = 0; ph ^= 1; }
+                        if (q_next && ++k == q_at) {
+                            if (!(ok = issue_q(un))) break;
+                            q_next = false;
+                        }
                     }
                 }
             }
@@ -522,6 +540,46 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
 
 int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 
+// Tiles of the busiest CTA when the n_rb x ceil(Nd/dpu) work units (unit u:
+// row block u % n_rb, documents [dpu*(u/n_rb), +dpu)) are dealt round-robin
+// to min(units, sms) persistent CTAs.  Only the last chunk of documents
+// can be short.
+int64_t busiest_tiles(int64_t n_rb, int64_t Nd, int64_t dpu, int64_t tiles, int64_t sms) {
+    const int64_t chunks = (Nd + dpu - 1) / dpu, n = n_rb * chunks;
+    const int64_t grid = n < sms ? n : sms;
+    const int64_t short_by = (chunks * dpu - Nd) * tiles;  // missing tiles of a last-chunk unit
+    const int64_t lo = n - n_rb;                           // first unit of the last chunk
+    int64_t most = 0;
+    for (int64_t b = 0; b < grid; ++b) {
+        const int64_t cnt = (n - 1 - b) / grid + 1;
+        const int64_t f = b >= lo ? b : b + ((lo - b + grid - 1) / grid) * grid;
+        const int64_t n_short = f < n ? (n - 1 - f) / grid + 1 : 0;
+        const int64_t load = cnt * dpu * tiles - n_short * short_by;
+        most = load > most ? load : most;
+    }
+    return most;
+}
+
+// Documents per work unit.  A unit costs one Q row-block load and a short
+// pipeline refill (about a quarter of a tile, measured), so units are kept
+// long (up to ~24 tiles) unless shorter ones even out the CTAs' loads.
+int choose_docs_per_unit(int64_t n_rb, int64_t Nd, int tiles, int sms) {
+    const int dmax = ceil_div(24, tiles);
+    int best = dmax;
+    double best_cost = 0.0;
+    for (int dpu = dmax; dpu >= 1; --dpu) {
+        const int64_t chunks = (Nd + dpu - 1) / dpu, n = n_rb * chunks;
+        const int64_t grid = n < sms ? n : sms;
+        const double units_busiest = static_cast<double>((n + grid - 1) / grid);
+        const double cost = static_cast<double>(busiest_tiles(n_rb, Nd, dpu, tiles, sms)) + 0.25 * units_busiest;
+        if (dpu == dmax || cost < best_cost) {
+            best = dpu;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 bool tc_allpairs_eligible(const Problem& P) {
@@ -560,10 +618,7 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
     p.stages = static_cast<int>(budget / p.d_bytes);
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return cudaErrorInvalidConfiguration;
-    // documents per work unit: ~24 tiles, but keep at least two units per SM
-    p.dpu = ceil_div(24, p.tiles_per_doc);
-    while (p.dpu > 1 && static_cast<int64_t>(p.n_rb) * ceil_div(P.n_doc, p.dpu) < 2LL * info.sm_count)
-        p.dpu = (p.dpu + 1) / 2;
+    p.dpu = choose_docs_per_unit(p.n_rb, P.n_doc, p.tiles_per_doc, info.sm_count);
     p.n_units = static_cast<int64_t>(p.n_rb) * ceil_div(P.n_doc, p.dpu);
     p.idesc = ptx::f16_idesc(kM, p.T, P.dtype == kBF16);
     p.qmask = P.qmask;
