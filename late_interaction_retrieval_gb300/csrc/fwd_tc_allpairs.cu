@@ -26,7 +26,7 @@
 //               warpgroups split each tile's 16-column units round-robin
 //               (unit u goes to group u % 4) and keep a running (max, argmax)
 //               per row; at the end of a document each group hands its
-//               values to the reducers through shared memory (two slots)
+//               values to the reducers through shared memory
 //               and goes on with the next document.
 //   warps 18,19 reducers: merge the four groups' values per row, sum each
 //               query's valid rows and write the score and argmax, while the
@@ -62,7 +62,7 @@ constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
 constexpr int kRedWarps = 2;          // document-end reducers
 constexpr int kThreads = 32 * (2 + kEpiWarps + kRedWarps);
-constexpr int kSlots = 2;             // documents in flight between the epilogue and the reducers
+constexpr int kSlots = 1;             // documents in flight between the epilogue and the reducers
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
 constexpr int kMaxDim = 256;        // largest embedding size the tensor-core paths take
