@@ -80,6 +80,8 @@ SWEEP = [
     ("allpairs",   2,  3,  5,   40,   96),
     ("allpairs",   4, 400, 32, 300,  128),  # 160-column tiles, 3 accumulators, several per CTA
     ("allpairs",   1, 700, 128, 140, 128),  # 144-column tiles, many per CTA
+    ("allpairs", 150,  3, 32,  200,   64),  # 4800 query tokens reach each document in the backward
+    ("allpairs",  40,  2, 128, 130,  128),  # 5120 of them, at Lq = 128
     ("pairwise",   7,  0, 32,  700,  128),
     ("pairwise",   4,  0, 20, 2100,  128),
     ("pairwise",   3,  0, 128, 129,   64),
