@@ -20,7 +20,7 @@
 //
 // Warp roles (640 threads, one CTA per SM, persistent over work units):
 //   warp 0      TMA producer: Q row blocks (2 buffers) and D tiles (S stages)
-//   warp 1      TMEM allocator + single-thread MMA issuer
+//   warp 1      TMEM allocator + MMA issuer of the even tiles
 //   warps 2..17 epilogue: four warpgroups; warp w reads TMEM lanes
 //               32*(w%4)..+31, i.e. one accumulator row per thread.  The
 //               warpgroups split each tile's 16-column units round-robin
@@ -28,9 +28,11 @@
 //               per row; at the end of a document each group hands its
 //               values to the reducers through shared memory
 //               and goes on with the next document.
-//   warps 18,19 reducers: merge the four groups' values per row, sum each
-//               query's valid rows and write the score and argmax, while the
+//   warp 18     reducer: merges the four groups' values per row, sums each
+//               query's valid rows and writes the score and argmax, while the
 //               epilogue and the MMA continue.
+//   warp 19     MMA issuer of the odd tiles (one issuing thread leaves the
+//               tensor pipe idle while it checks barriers between chains)
 // The accumulator is multi-buffered in TMEM (512 columns split into 2..4
 // buffers, as many as the tile width allows), so the MMA runs ahead of the
 // epilogue.
@@ -60,8 +62,9 @@ namespace {
 
 constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
-constexpr int kRedWarps = 2;          // document-end reducers
-constexpr int kThreads = 32 * (2 + kEpiWarps + kRedWarps);
+constexpr int kRedWarps = 1;          // document-end reducer
+constexpr int kIssuers = 2;           // MMA issuing threads (warp 1 and the last warp)
+constexpr int kThreads = 32 * (2 + kEpiWarps + kRedWarps + 1);
 constexpr int kSlots = 1;             // documents in flight between the epilogue and the reducers
 constexpr int kM = 128;              // accumulator rows (query tokens) per tile
 constexpr int kAtomBytes = 128;      // one 128-byte swizzle row = 64 fp16/bf16
@@ -229,7 +232,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->full_q[b]), 1);
-            ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), 1);
+            ptx::mbar_init(ptx::smem_u32(&bars->empty_q[b]), kIssuers);
         }
         for (int b = 0; b < kMaxAcc; ++b) {
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
@@ -240,7 +243,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::mbar_init(ptx::smem_u32(&bars->xfree[b]), kRedWarps * 32);
             ptx::mbar_init(ptx::smem_u32(&bars->rsum[b]), kRedWarps * 32);
         }
-        ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->mma_done), kIssuers);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -318,12 +321,21 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 if (issued_q & (1u << k))
                     ptx::mbar_wait(ptx::smem_u32(&bars->full_q[k]), (last_ph_q >> k) & 1u, err);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3 + kEpiWarps) {
         // ----------------------------------------------------------- MMA --
+        // Two issuing threads take alternate tiles.  Issuing a chain blocks
+        // until the tensor pipe has room, so a single thread is only a few
+        // MMAs ahead of the pipe, and its barrier checks between chains (a few
+        // hundred cycles) would leave the pipe idle; with two threads one
+        // thread's chain runs while the other checks its barriers.  Each thread
+        // commits its own tiles; at the end of every unit both arrive on the
+        // unit's Q buffer, and both on the final drain barrier.
         if (lane == 0) {
+            const int who = warp == 1 ? 0 : 1;
             int s = 0, qb = 0, ab = 0;
             uint32_t ph = 0, qph = 0, aph = 0;
             bool ok = true;
+            int64_t k = 0;  // tile index in this CTA's sequence
             for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
                 const int64_t d0 = (u / p.n_rb) * p.dpu;
                 const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
@@ -331,19 +343,21 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 ptx::tc_fence_after();
                 const uint32_t qaddr = ptx::smem_u32(qbuf + qb * p.q_bytes);
                 for (int64_t d = d0; ok && d < d1; ++d) {
-                    for (int t = 0; t < p.tiles_per_doc; ++t) {
-                        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph, err))) break;
-                        if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[ab]), aph ^ 1, err))) break;
-                        ptx::tc_fence_after();
-                        const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
-                        const uint32_t acc = tmem_base + ab * p.acc_stride;
-                        if (p.dim == 128)  // the common embedding size: no per-step guards
-                            ptx::mma_kchain<8>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes, 8, p.idesc);
-                        else
-                            ptx::mma_kchain<kMaxDim / 16>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes,
-                                                          p.dim / 16, p.idesc);
-                        ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
-                        ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
+                    for (int t = 0; t < p.tiles_per_doc; ++t, ++k) {
+                        if ((k & 1) == who) {
+                            if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph, err))) break;
+                            if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[ab]), aph ^ 1, err))) break;
+                            ptx::tc_fence_after();
+                            const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
+                            const uint32_t acc = tmem_base + ab * p.acc_stride;
+                            if (p.dim == 128)  // the common embedding size: no per-step guards
+                                ptx::mma_kchain<8>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes, 8, p.idesc);
+                            else
+                                ptx::mma_kchain<kMaxDim / 16>(acc, qaddr, kM * kAtomBytes, daddr, p.T * kAtomBytes,
+                                                              p.dim / 16, p.idesc);
+                            ptx::mma_commit(ptx::smem_u32(&bars->empty_d[s]));
+                            ptx::mma_commit(ptx::smem_u32(&bars->acc_full[ab]));
+                        }
                         if (++s == p.stages) { s = 0; ph ^= 1; }
                         if (++ab == p.nacc) { ab = 0; aph ^= 1; }
                     }
@@ -351,7 +365,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 ptx::mma_commit(ptx::smem_u32(&bars->empty_q[qb]));
                 if (++qb == 2) { qb = 0; qph ^= 1; }
             }
-            // all MMAs this thread issued complete before TMEM is released
+            // all MMAs of both threads complete before TMEM is released
             ptx::mma_commit(ptx::smem_u32(&bars->mma_done));
             ptx::mbar_wait(ptx::smem_u32(&bars->mma_done), 0, err);
         }
@@ -450,28 +464,48 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         // Per document: merge the warpgroups' (max, argmax) per row (strictly
         // greater wins, equal maxima keep the lower column), sum the valid
         // query tokens' maxima per query in a fixed order, write score and
-        // argmax.  A thread owns rows rr and rr + 64.
+        // argmax.  A thread owns rows rr + 32 * kRedWarps * k.
         constexpr int kRows = kM / (32 * kRedWarps);
-        const int rr = (warp - 2 - kEpiWarps) * 32 + lane;
+        const int rr = (warp - 2 - kEpiWarps) * 32 + lane;  // the reducer warp(s) follow the epilogue
         const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
         int slot = 0;
         uint32_t xph = 0;
         bool ok = true;
+        // position of each owned row inside its query (the same in every unit)
+        int qloc[kRows], iq[kRows];
+#pragma unroll
+        for (int k = 0; k < kRows; ++k) {
+            const int r = rr + k * 32 * kRedWarps;
+            qloc[k] = static_cast<int>(r / Lq);
+            iq[k] = static_cast<int>(r - static_cast<int64_t>(qloc[k]) * Lq);
+        }
+        // query-mask bytes of a unit's rows (0 for rows past the last query);
+        // the next unit's are loaded one unit ahead, off the document-end path
+        auto load_qvalid = [&](int64_t uu, uint8_t (&out)[kRows]) {
+            const int64_t rbq = uu % p.n_rb;
+#pragma unroll
+            for (int k = 0; k < kRows; ++k) {
+                const int r = rr + k * 32 * kRedWarps;
+                const int64_t qq = rbq * p.qpt + qloc[k];
+                const bool in = r < qrows && qq < p.Nq;
+                out[k] = in ? (p.qmask ? p.qmask[qq * Lq + iq[k]] : uint8_t(1)) : uint8_t(0);
+            }
+        };
+        uint8_t qv_cur[kRows], qv_next[kRows];
+        if (blockIdx.x < p.n_units) load_qvalid(blockIdx.x, qv_cur);
         for (int64_t u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+            if (u + gridDim.x < p.n_units) load_qvalid(u + gridDim.x, qv_next);
             const int rb = static_cast<int>(u % p.n_rb);
             const int64_t d0 = (u / p.n_rb) * p.dpu;
             const int64_t d1 = d0 + p.dpu < p.Nd ? d0 + p.dpu : p.Nd;
             int64_t q[kRows];
-            int iq[kRows];
             bool row_ok[kRows], qvalid[kRows];
 #pragma unroll
             for (int k = 0; k < kRows; ++k) {
                 const int r = rr + k * 32 * kRedWarps;
-                const int qloc = static_cast<int>(r / Lq);
-                iq[k] = static_cast<int>(r - static_cast<int64_t>(qloc) * Lq);
-                q[k] = static_cast<int64_t>(rb) * p.qpt + qloc;
+                q[k] = static_cast<int64_t>(rb) * p.qpt + qloc[k];
                 row_ok[k] = r < qrows && q[k] < p.Nq;
-                qvalid[k] = row_ok[k] && (!p.qmask || p.qmask[q[k] * Lq + iq[k]]);
+                qvalid[k] = qv_cur[k] != 0;
             }
             for (int64_t d = d0; ok && d < d1; ++d) {
                 ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull[slot]), xph, err);
@@ -527,6 +561,8 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 }
                 if (++slot == kSlots) { slot = 0; xph ^= 1; }
             }
+#pragma unroll
+            for (int k = 0; k < kRows; ++k) qv_cur[k] = qv_next[k];
         }
     }
 
