@@ -176,7 +176,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the liblik calls of one step of a workload."""
 
-    def __init__(self, name: str, device: torch.device):
+    def __init__(self, name: str, device: torch.device, grad_dtype: str = "f32"):
         from late_interaction_retrieval_gb300 import binding
         self.binding = binding
         self.w = W.WORKLOADS[name]
@@ -187,8 +187,11 @@ class Step:
         self.scores = torch.empty(w.score_shape, dtype=torch.float32, device=device)
         self.argmax = (torch.empty((*w.score_shape, w.lq), dtype=torch.int32, device=device)
                        if w.backward else None)
-        self.gQ = torch.empty(i.Q.shape, dtype=torch.float32, device=device) if w.backward else None
-        self.gD = torch.empty(i.D.shape, dtype=torch.float32, device=device) if w.backward else None
+        # gradients in fp32 (the default entry points) or in the inputs' dtype
+        self.same_dtype = grad_dtype == "input"
+        gdt = i.Q.dtype if self.same_dtype else torch.float32
+        self.gQ = torch.empty(i.Q.shape, dtype=gdt, device=device) if w.backward else None
+        self.gD = torch.empty(i.D.shape, dtype=gdt, device=device) if w.backward else None
         self.fwd()
         torch.cuda.synchronize()
         if w.backward:
@@ -208,7 +211,7 @@ class Step:
 
     def bwd(self, Q=None, D=None, g=None):
         i = self.inp
-        getattr(self.binding, f"lik_maxsim_{self.layout}_bwd")(
+        getattr(self.binding, f"lik_maxsim_{self.layout}_bwd" + ("_same_dtype" if self.same_dtype else ""))(
             i.Q if Q is None else Q, i.D if D is None else D, self.g if g is None else g,
             self.argmax, self.gQ, self.gD)
 
@@ -251,7 +254,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     name = args.workload
-    st = Step(name, device)
+    st = Step(name, device, args.grad_dtype)
     w = st.w
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -340,6 +343,7 @@ def run_ours(args):
             "config": {
                 "workload": name, "layout": w.layout,
                 "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
+                "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
                 "counted_flops_per_step": counted, "valid_token_flops_per_step": st.valid_flops(),
                 "algorithmic_fwd_bytes": st.algorithmic_bytes(),
                 "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -515,6 +519,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="inbatch_b128_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--grad-dtype", choices=["f32", "input"], default="f32",
+                    help="gradients in fp32 (default) or in the inputs' dtype (the _bwd_same_dtype entry points)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

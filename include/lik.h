@@ -172,6 +172,37 @@ lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype,
                              const float* grad_out, const int32_t* argmax,
                              float* grad_Q, float* grad_D, cudaStream_t stream);
 
+/* ------------------------------------------- gradients in the inputs' dtype --
+ * The same backward with grad_Q and grad_D in the dtype of Q and D instead of
+ * fp32, so a bf16/fp16 training step keeps no fp32 gradient buffers and writes
+ * half the bytes (colpali PR "Add support for late-interaction-kernels
+ * (LIK)", Results: the fused backward allocates only the input gradients,
+ * and its cost is dominated by writing grad_D).  Every element is summed in
+ * fp32 and rounded to the output type once (round to nearest even); each
+ * row of grad_D is written exactly once, zeros included.
+ *   - fp32 inputs: identical to the fp32 entry points.
+ *   - fp16/bf16 inputs: need dim % 8 == 0 and dim <= 256, else
+ *     LIK_ERR_UNSUPPORTED (the fp32-gradient entry points take any dim).
+ *   - grad_Q, grad_D: same shapes as Q and D, dtype of Q and D, 16-byte
+ *     aligned, overwritten; NULL to skip.  Other arguments and errors as in
+ *     the fp32-gradient entry points above.
+ */
+lik_status lik_maxsim_allpairs_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype,
+                                              int64_t Nq, int64_t Nd, int64_t Lq, int64_t Ld,
+                                              int64_t dim, const float* grad_out,
+                                              const int32_t* argmax, void* grad_Q, void* grad_D,
+                                              cudaStream_t stream);
+
+lik_status lik_maxsim_pairwise_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype,
+                                              int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
+                                              const float* grad_out, const int32_t* argmax,
+                                              void* grad_Q, void* grad_D, cudaStream_t stream);
+
+lik_status lik_maxsim_kd_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                        int64_t N, int64_t Lq, int64_t Ld, int64_t dim,
+                                        const float* grad_out, const int32_t* argmax,
+                                        void* grad_Q, void* grad_D, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -34,6 +34,9 @@ SIGNATURES = {
     "lik_maxsim_pairwise_bwd": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
     "lik_maxsim_kd_fwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_kd_bwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_allpairs_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_pairwise_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
+    "lik_maxsim_kd_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
 }
 
 _DTYPES = {torch.float32: LIK_F32, torch.float16: LIK_F16, torch.bfloat16: LIK_BF16}
@@ -209,6 +212,47 @@ def lik_maxsim_kd_bwd(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=N
     _need(grad_Q, "grad_Q", (B, Lq, dim), torch.float32, dev, optional=True)
     _need(grad_D, "grad_D", (B, N, Ld, dim), torch.float32, dev, optional=True)
     _check(load().lik_maxsim_kd_bwd(
+        _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+# ------------------------------------------- gradients in the inputs' dtype --
+
+def lik_maxsim_allpairs_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    Nq, Lq, dim = Q.shape
+    Nd, Ld, _ = D.shape
+    _need(grad_out, "grad_out", (Nq, Nd), torch.float32, dev)
+    _need(argmax, "argmax", (Nq, Nd, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (Nq, Lq, dim), Q.dtype, dev, optional=True)
+    _need(grad_D, "grad_D", (Nd, Ld, dim), Q.dtype, dev, optional=True)
+    _check(load().lik_maxsim_allpairs_bwd_same_dtype(
+        _ptr(Q), _ptr(D), dt, Nq, Nd, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+def lik_maxsim_pairwise_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 3)
+    B, Lq, dim = Q.shape
+    Ld = D.shape[1]
+    _need(grad_out, "grad_out", (B,), torch.float32, dev)
+    _need(argmax, "argmax", (B, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (B, Lq, dim), Q.dtype, dev, optional=True)
+    _need(grad_D, "grad_D", (B, Ld, dim), Q.dtype, dev, optional=True)
+    _check(load().lik_maxsim_pairwise_bwd_same_dtype(
+        _ptr(Q), _ptr(D), dt, B, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+def lik_maxsim_kd_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
+    dt, dev = _embeddings(Q, D, 3, 4)
+    B, Lq, dim = Q.shape
+    N, Ld = D.shape[1], D.shape[2]
+    _need(grad_out, "grad_out", (B, N), torch.float32, dev)
+    _need(argmax, "argmax", (B, N, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", (B, Lq, dim), Q.dtype, dev, optional=True)
+    _need(grad_D, "grad_D", (B, N, Ld, dim), Q.dtype, dev, optional=True)
+    _check(load().lik_maxsim_kd_bwd_same_dtype(
         _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
         _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
 

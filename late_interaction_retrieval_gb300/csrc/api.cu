@@ -255,6 +255,45 @@ lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argma
     return LIK_OK;
 }
 
+// Backward with grad_Q / grad_D in the inputs' dtype.  fp32 inputs take the
+// fp32 path unchanged.
+lik_status run_bwd_same(const Problem& P, const float* grad_out, const int32_t* argmax, void* grad_Q,
+                        void* grad_D, cudaStream_t stream) {
+    if (P.dtype == kF32)
+        return run_bwd(P, grad_out, argmax, static_cast<float*>(grad_Q), static_cast<float*>(grad_D), stream);
+    int dev = 0;
+    lik_status st = check_device(&dev);
+    if (st != LIK_OK) return st;
+    if (!bwd_same_dtype_supported(P))
+        return fail(LIK_ERR_UNSUPPORTED,
+                    "the backward with fp16/bf16 gradients needs dim %% 8 == 0 and dim <= 256 "
+                    "(the fp32-gradient entry point takes any dim)");
+    const int64_t q_elems = P.n_query * P.Lq * P.dim, d_elems = P.n_doc * P.Ld * P.dim;
+    const bool need_hits = P.n_pairs * P.Lq > 0 && (grad_Q || grad_D);
+    if (need_hits && !argmax) return fail(LIK_ERR_INVALID_ARG, "argmax is NULL");
+    if (need_hits && !grad_out) return fail(LIK_ERR_INVALID_ARG, "grad_out is NULL");
+    const Spec specs[] = {
+        {"Q", P.Q, grad_D != nullptr, q_elems},
+        {"D", P.D, grad_Q != nullptr, d_elems},
+        {"grad_out", grad_out, false, P.n_pairs},
+        {"argmax", argmax, false, P.n_pairs * P.Lq},
+        {"grad_Q", grad_Q, false, q_elems},
+        {"grad_D", grad_D, false, d_elems},
+    };
+    if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
+    if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
+    if ((st = check_aligned(grad_out, 4, "grad_out")) != LIK_OK) return st;
+    if ((st = check_aligned(argmax, 4, "argmax")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_Q, 16, "grad_Q")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_D, 16, "grad_D")) != LIK_OK) return st;
+    cudaError_t e;
+    if (grad_Q && (e = launch_bwd_grad_q_same(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess)
+        return cuda_fail(e, "grad_Q launch");
+    if (grad_D && (e = launch_bwd_grad_d_same(P, grad_out, argmax, grad_D, stream)) != cudaSuccess)
+        return cuda_fail(e, "grad_D launch");
+    return LIK_OK;
+}
+
 }  // namespace
 }  // namespace lik
 
@@ -372,6 +411,44 @@ lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype, int6
     Problem P = make_problem(kKd, dtype, Q, D, nullptr, nullptr, B, B * N, N, B * N, Lq, Ld, dim);
     if (nothing) P.n_pairs = 0;
     return run_bwd(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_allpairs_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
+                                              int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,
+                                              const float* grad_out, const int32_t* argmax, void* grad_Q,
+                                              void* grad_D, cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, Nq, Nd, Nd, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kAllPairs, dtype, Q, D, nullptr, nullptr, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+    if (nothing) P.n_pairs = 0;
+    return run_bwd_same(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_pairwise_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                              int64_t Lq, int64_t Ld, int64_t dim, const float* grad_out,
+                                              const int32_t* argmax, void* grad_Q, void* grad_D,
+                                              cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kPairwise, dtype, Q, D, nullptr, nullptr, B, B, 1, B, Lq, Ld, dim);
+    return run_bwd_same(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_kd_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                                        int64_t Lq, int64_t Ld, int64_t dim, const float* grad_out,
+                                        const int32_t* argmax, void* grad_Q, void* grad_D,
+                                        cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kKd, dtype, Q, D, nullptr, nullptr, B, B * N, N, B * N, Lq, Ld, dim);
+    if (nothing) P.n_pairs = 0;
+    return run_bwd_same(P, grad_out, argmax, grad_Q, grad_D, stream);
 }
 
 }  // extern "C"

@@ -66,11 +66,33 @@ struct Raw8<float> {
     }
 };
 
+// Gradient outputs: fp32, or the inputs' 16-bit type (rounded to nearest
+// even once, from the fp32 sum).
+__device__ __forceinline__ void store8(float* out, const float (&o)[8]) {
+    *reinterpret_cast<float4*>(out) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(out + 4) = make_float4(o[4], o[5], o[6], o[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* out, const float (&o)[8]) {
+    __nv_bfloat162 h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(h);
+}
+__device__ __forceinline__ void store8(__half* out, const float (&o)[8]) {
+    __half2 h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = __floats2half2_rn(o[2 * e], o[2 * e + 1]);
+    *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(h);
+}
+__device__ __forceinline__ void store1(float* out, float v) { *out = v; }
+__device__ __forceinline__ void store1(__nv_bfloat16* out, float v) { *out = __float2bfloat16_rn(v); }
+__device__ __forceinline__ void store1(__half* out, float v) { *out = __float2half_rn(v); }
+
 // VECS vectors of 8 elements per thread: dim <= VECS * 64.
-template <typename T, int VECS, int kUnroll>
+template <typename T, int VECS, int kUnroll, typename TO>
 __global__ void __launch_bounds__(kVecThreads)
 grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
-                  float* __restrict__ gQ, unsigned int* err) {
+                  TO* __restrict__ gQ, unsigned int* err) {
     __shared__ int s_am[kPairChunk][kRowsPerCta];
     __shared__ float s_g[kPairChunk];
     __shared__ float s_part[kRowsPerCta][VECS * kThreadsPerRow * kVec];
@@ -142,7 +164,7 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
     }
     __syncthreads();
     if (pg == 1 || r >= rows_here) return;
-    float* out = gQ + (q * P.Lq + i0 + r) * P.dim;
+    TO* out = gQ + (q * P.Lq + i0 + r) * P.dim;
 #pragma unroll
     for (int m = 0; m < VECS; ++m) {
         const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
@@ -150,16 +172,15 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
         float o[kVec];
 #pragma unroll
         for (int e = 0; e < kVec; ++e) o[e] = acc[m][e] + s_part[r][k + e];
-        *reinterpret_cast<float4*>(out + k) = make_float4(o[0], o[1], o[2], o[3]);
-        *reinterpret_cast<float4*>(out + k + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        store8(out + k, o);
     }
 }
 
 // Any-dim path: one warp per (query, token) row; lanes stride over dim.
-template <typename T>
+template <typename T, typename TO>
 __global__ void __launch_bounds__(kThreads)
 grad_q_gather_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
-                     float* __restrict__ gQ, unsigned int* err) {
+                     TO* __restrict__ gQ, unsigned int* err) {
     const T* D = static_cast<const T*>(P.D);
     const int lane = threadIdx.x & 31;
     const int64_t rows = P.n_query * P.Lq;
@@ -187,7 +208,7 @@ grad_q_gather_kernel(Problem P, const float* __restrict__ g, const int32_t* __re
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 const int64_t k = k0 + lane + 32 * m;
-                if (k < P.dim) gQ[row * P.dim + k] = acc[m];
+                if (k < P.dim) store1(gQ + row * P.dim + k, acc[m]);
             }
         }
     }
@@ -302,6 +323,328 @@ grad_d_scatter_atomic_kernel(Problem P, const float* __restrict__ g,
     }
 }
 
+// ------------------------------------------- grad_D in the inputs' dtype --
+//
+// A 16-bit grad_D cannot be accumulated with global atomics without rounding
+// at every addition, so these kernels sum each row's hits in fp32 (registers
+// or shared memory) and write every row exactly once (zeros included: no
+// zero-fill).  dim % 8 == 0, dim <= 256.
+
+constexpr int kOwnRowThreads = 16;                        // threads sharing one grad_D row
+constexpr int kOwnSlots = kThreads / kOwnRowThreads;      // rows handled at once by a CTA
+
+// Pairwise and kd (one pair per document, Lq <= 32): one CTA per document.
+// Warp 0 ranks the pair's hits by (row, token) into shared memory; the CTA
+// then walks the document's rows in order, each row-slot keeping a cursor
+// into the sorted hits, and writes every row.
+template <typename T, int VECS, typename TO>
+__global__ void __launch_bounds__(kThreads)
+grad_d_doc_stream_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                         TO* __restrict__ gD, unsigned int* err) {
+    __shared__ int s_row[32], s_qrow[32], s_nh;
+    __shared__ float s_g;
+    const T* Q = static_cast<const T*>(P.Q);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slot = threadIdx.x / kOwnRowThreads, sub = threadIdx.x % kOwnRowThreads;
+    const int Lq = static_cast<int>(P.Lq);
+    for (int64_t dd = blockIdx.x; dd < P.n_doc; dd += gridDim.x) {
+        if (warp == 0) {
+            int32_t a = lane < Lq ? am[dd * Lq + lane] : -1;
+            if (a >= P.Ld) {
+                atomicOr(err, kErrBadIndex);
+                a = -1;
+            }
+            const unsigned valid = __ballot_sync(0xffffffffu, a >= 0);
+            int rank = 0;
+            for (int o = 0; o < 32; ++o) {
+                const int32_t ao = __shfl_sync(0xffffffffu, a, o);
+                rank += ((valid >> o) & 1u) && (ao < a || (ao == a && o < lane)) ? 1 : 0;
+            }
+            if (a >= 0) {
+                s_row[rank] = a;
+                s_qrow[rank] = static_cast<int>(P.query_of(dd) * Lq + lane);
+            }
+            if (lane == 0) {
+                s_nh = __popc(valid);
+                s_g = valid ? g[dd] : 0.f;
+            }
+        }
+        __syncthreads();
+        const int nh = s_nh;
+        const float gv = s_g;
+        TO* base = gD + dd * P.Ld * P.dim;
+        int ptr = 0;
+        for (int64_t j = slot; j < P.Ld; j += kOwnSlots) {
+            while (ptr < nh && s_row[ptr] < j) ++ptr;
+            float acc[VECS][kVec];
+#pragma unroll
+            for (int m = 0; m < VECS; ++m)
+#pragma unroll
+                for (int e = 0; e < kVec; ++e) acc[m][e] = 0.f;
+            for (int h = ptr; h < nh && s_row[h] == j; ++h) {
+                const T* src = Q + static_cast<int64_t>(s_qrow[h]) * P.dim;
+#pragma unroll
+                for (int m = 0; m < VECS; ++m) {
+                    const int64_t kk = static_cast<int64_t>(m * kOwnRowThreads + sub) * kVec;
+                    if (kk >= P.dim) break;
+                    Raw8<T> x;
+                    x.load(src + kk);
+#pragma unroll
+                    for (int e = 0; e < kVec; ++e) acc[m][e] = fmaf(gv, x.get(e), acc[m][e]);
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < VECS; ++m) {
+                const int64_t kk = static_cast<int64_t>(m * kOwnRowThreads + sub) * kVec;
+                if (kk >= P.dim) break;
+                store8(base + j * P.dim + kk, acc[m]);
+            }
+        }
+        __syncthreads();  // s_row, s_qrow, s_nh and s_g are rewritten for the next document
+    }
+}
+
+// All-pairs (and pairwise/kd with Lq > 32): one CTA owns a block of rows of
+// one document and keeps their fp32 sums in shared memory (64 KB: 16384 /
+// dim rows).  Per round of kChunkRound hits (the (pair, token) entries that
+// use the document), the CTA stages each hit's row within the block (or -1)
+// in shared memory; warp w then adds the Q rows of the hits on the block's
+// rows r with r % 8 == w, four hits' rows loaded at once, with plain float4
+// read-modify-writes: no two warps touch one row, and one lane's updates of a
+// row are in program order, so no atomics are needed.  Every row of the block
+// is written once at the end.
+constexpr int kChunkFloats = 16384;                        // 64 KB of fp32 sums per CTA
+constexpr int kChunkRound = 4096;                          // hits staged per round
+
+template <typename T, typename TO>
+__global__ void __launch_bounds__(kThreads)
+grad_d_chunk_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                    TO* __restrict__ gD, int64_t rows_per_cta, int64_t chunks, unsigned int* err) {
+    extern __shared__ float s_acc[];                              // rows x dim
+    int* s_row = reinterpret_cast<int*>(s_acc + kChunkFloats);  // [kChunkRound]
+    const T* Q = static_cast<const T*>(P.Q);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t dd = blockIdx.x / chunks;
+    const int64_t j0 = (static_cast<int64_t>(blockIdx.x) - dd * chunks) * rows_per_cta;
+    const int rows = static_cast<int>(P.Ld - j0 < rows_per_cta ? P.Ld - j0 : rows_per_cta);
+    const int dim = static_cast<int>(P.dim);
+    const bool all = P.layout == kAllPairs;
+    const int64_t K = all ? P.n_query : 1;            // pairs that use document dd
+    const int64_t q_one = all ? 0 : P.query_of(dd);  // their query when there is one pair
+    const int Lq = static_cast<int>(P.Lq);
+    const int total = static_cast<int>(K * Lq);       // hits e = k * Lq + i (host: K * Lq < 2^31)
+    bool bad = false;
+
+    for (int x = threadIdx.x * 4; x < rows * dim; x += kThreads * 4)
+        *reinterpret_cast<float4*>(s_acc + x) = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    for (int e0 = 0; e0 < total; e0 += kChunkRound) {
+        __syncthreads();  // the previous round's rows are consumed (and the zero-fill is done)
+#pragma unroll 4
+        for (int t = threadIdx.x; t < kChunkRound; t += kThreads) {
+            const int e = e0 + t;
+            int32_t a = -1;
+            if (e < total) {
+                const int k = e / Lq, i = e - k * Lq;
+                a = am[((all ? k * P.pairs_per_query : 0) + dd) * Lq + i];
+            }
+            if (a >= P.Ld) bad = true;
+            const int64_t r = static_cast<int64_t>(a) - j0;
+            s_row[t] = (a >= 0 && a < P.Ld && r >= 0 && r < rows) ? static_cast<int>(r) : -1;
+        }
+        __syncthreads();
+        for (int t0 = 0; t0 < kChunkRound; t0 += 32) {
+            const int my_row = s_row[t0 + lane];
+            unsigned live = __ballot_sync(0xffffffffu, my_row >= 0 && (my_row & (kWarps - 1)) == warp);
+            while (live) {
+                int src[4], rr[4];
+                float gv[4];
+                const T* qr[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    src[u] = live ? __ffs(live) - 1 : -1;
+                    if (src[u] >= 0) live &= live - 1;
+                    const int sl = src[u] >= 0 ? src[u] : 0;
+                    rr[u] = __shfl_sync(0xffffffffu, my_row, sl);
+                    const int e = e0 + t0 + sl;
+                    const int k = e / Lq, i = e - k * Lq;
+                    const int64_t pair = all ? k * P.pairs_per_query + dd : dd;
+                    gv[u] = src[u] >= 0 ? g[pair] : 0.f;
+                    qr[u] = Q + ((all ? k : q_one) * Lq + i) * static_cast<int64_t>(dim);
+                }
+                for (int k0 = lane * 4; k0 < dim; k0 += 128) {
+                    float x[4][4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (src[u] >= 0) load4(qr[u] + k0, x[u]);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (src[u] >= 0) {
+                            float4* dst = reinterpret_cast<float4*>(s_acc + rr[u] * dim + k0);
+                            float4 v = *dst;
+                            v.x = fmaf(gv[u], x[u][0], v.x);
+                            v.y = fmaf(gv[u], x[u][1], v.y);
+                            v.z = fmaf(gv[u], x[u][2], v.z);
+                            v.w = fmaf(gv[u], x[u][3], v.w);
+                            *dst = v;
+                        }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    TO* out = gD + (dd * P.Ld + j0) * P.dim;
+    for (int x = threadIdx.x * kVec; x < rows * dim; x += kThreads * kVec) {
+        float o[kVec];
+#pragma unroll
+        for (int c = 0; c < kVec; ++c) o[c] = s_acc[x + c];
+        store8(out + x, o);
+    }
+    if (bad) atomicOr(err, kErrBadIndex);
+}
+
+// All-pairs with at most kOwnWindow hits per document (Nq * Lq <= 4096):
+// document-owner gather.  One CTA owns kOwnRows rows of one document.  Each
+// thread reads 16 of the document's argmax entries into registers (all loads
+// in flight together); the hits that land in the CTA's rows are bucketed by a
+// stable counting sort in shared memory (per-warp counts, a block-wide scan,
+// ranks among equal rows from __match_any_sync); then 16 threads per row sum
+// the row's hits in fp32 registers, four row loads in flight, and write the
+// row once.  The bucket order depends only on the data: bit-reproducible.
+constexpr int kOwnRows = 128;                              // rows of grad_D per CTA
+constexpr int kOwnHitsPerThread = 16;
+constexpr int kOwnWindow = kOwnHitsPerThread * kThreads;   // 4096 hits
+
+template <typename T, int VECS, typename TO>
+__global__ void __launch_bounds__(kThreads, 3)
+grad_d_owner_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                    TO* __restrict__ gD, int64_t chunks, unsigned int* err) {
+    __shared__ int2 s_hit[kOwnWindow];             // (Q row, pair) in bucket order
+    __shared__ int s_cnt[kOwnRows * kWarps];       // per (row, warp), row-major; then offsets
+    __shared__ int s_start[kOwnRows + 1];          // first hit of each row in s_hit
+    __shared__ int s_wsum[kWarps];
+    static_assert(kWarps == 8 && kOwnRows * kWarps == 4 * kThreads, "scan layout");
+    const T* Q = static_cast<const T*>(P.Q);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t dd = blockIdx.x / chunks;
+    const int64_t j0 = (static_cast<int64_t>(blockIdx.x) - dd * chunks) * kOwnRows;
+    const int rows = static_cast<int>(P.Ld - j0 < kOwnRows ? P.Ld - j0 : kOwnRows);
+    const int Lq = static_cast<int>(P.Lq);
+    const int total = static_cast<int>(P.n_query * Lq);  // hits e = q * Lq + i (host: <= kOwnWindow)
+    const int slot = threadIdx.x / kOwnRowThreads, sub = threadIdx.x % kOwnRowThreads;
+    bool bad = false;
+
+    // ---- this thread's hits, all loads in flight together
+    int row[kOwnHitsPerThread];  // row within the block, or -1
+#pragma unroll
+    for (int m = 0; m < kOwnHitsPerThread; ++m) {
+        const int e = m * kThreads + static_cast<int>(threadIdx.x);
+        int32_t a = -1;
+        if (e < total) {
+            const int q = e / Lq, i = e - q * Lq;
+            a = am[(q * P.pairs_per_query + dd) * Lq + i];
+        }
+        row[m] = a;
+    }
+    for (int e = threadIdx.x; e < kOwnRows * kWarps; e += kThreads) s_cnt[e] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int m = 0; m < kOwnHitsPerThread; ++m) {
+        const int32_t a = row[m];
+        if (a >= P.Ld) bad = true;
+        const int64_t r = static_cast<int64_t>(a) - j0;
+        row[m] = (a >= 0 && a < P.Ld && r >= 0 && r < rows) ? static_cast<int>(r) : -1;
+        if (row[m] >= 0) atomicAdd(&s_cnt[row[m] * kWarps + warp], 1);
+    }
+    __syncthreads();
+
+    // ---- exclusive scan over (row, warp) in row-major order, 4 entries per thread
+    {
+        const int t = threadIdx.x;
+        const int v0 = s_cnt[4 * t], v1 = s_cnt[4 * t + 1], v2 = s_cnt[4 * t + 2], v3 = s_cnt[4 * t + 3];
+        const int tsum = v0 + v1 + v2 + v3;
+        int x = tsum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
+        }
+        if (lane == 31) s_wsum[warp] = x;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += s_wsum[w];
+        const int excl = base + x - tsum;
+        s_cnt[4 * t] = excl;
+        s_cnt[4 * t + 1] = excl + v0;
+        s_cnt[4 * t + 2] = excl + v0 + v1;
+        s_cnt[4 * t + 3] = excl + v0 + v1 + v2;
+        if ((t & 1) == 0) s_start[t >> 1] = excl;  // entry (row t/2, warp 0)
+        if (t == kThreads - 1) s_start[kOwnRows] = excl + tsum;
+    }
+    __syncthreads();
+
+    // ---- place, batch by batch in a fixed order; equal rows ranked by lane
+#pragma unroll
+    for (int m = 0; m < kOwnHitsPerThread; ++m) {
+        const bool in = row[m] >= 0;
+        const int key = in ? row[m] : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, key);
+        if (in) {
+            const int pos = s_cnt[key * kWarps + warp] + __popc(peers & ((1u << lane) - 1u));
+            const int e = m * kThreads + static_cast<int>(threadIdx.x);
+            const int q = e / Lq;
+            s_hit[pos] = make_int2(e, static_cast<int>(q * P.pairs_per_query + dd));
+        }
+        __syncwarp();
+        if (in && lane == __ffs(peers) - 1) s_cnt[key * kWarps + warp] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // ---- sum each row's hits in bucket order and write the row (zeros included)
+    for (int r = slot; r < rows; r += kOwnSlots) {
+        const int hs = s_start[r], he = s_start[r + 1];
+        float acc[VECS][kVec];
+#pragma unroll
+        for (int m = 0; m < VECS; ++m)
+#pragma unroll
+            for (int c = 0; c < kVec; ++c) acc[m][c] = 0.f;
+        for (int h = hs; h < he; h += 4) {
+            const T* src[4];
+            float gu[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const bool live = h + u < he;
+                const int2 hv = live ? s_hit[h + u] : make_int2(0, 0);
+                src[u] = live ? Q + static_cast<int64_t>(hv.x) * P.dim : nullptr;  // Q row q*Lq+i = e
+                gu[u] = live ? g[hv.y] : 0.f;
+            }
+#pragma unroll
+            for (int m = 0; m < VECS; ++m) {
+                const int64_t kk = static_cast<int64_t>(m * kOwnRowThreads + sub) * kVec;
+                if (kk >= P.dim) break;
+                Raw8<T> x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (src[u]) x[u].load(src[u] + kk);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (src[u])
+#pragma unroll
+                        for (int c = 0; c < kVec; ++c) acc[m][c] = fmaf(gu[u], x[u].get(c), acc[m][c]);
+            }
+        }
+        TO* out = gD + ((dd * P.Ld) + j0 + r) * P.dim;
+#pragma unroll
+        for (int m = 0; m < VECS; ++m) {
+            const int64_t kk = static_cast<int64_t>(m * kOwnRowThreads + sub) * kVec;
+            if (kk >= P.dim) break;
+            store8(out + kk, acc[m]);
+        }
+    }
+    if (bad) atomicOr(err, kErrBadIndex);
+}
+
 unsigned grid_for(int64_t warps_of_work, int per_sm) {
     int dev = 0;
     cudaGetDevice(&dev);
@@ -312,20 +655,20 @@ unsigned grid_for(int64_t warps_of_work, int per_sm) {
     return static_cast<unsigned>(blocks);
 }
 
-template <typename T>
-cudaError_t grad_q_typed(const Problem& P, const float* g, const int32_t* am, float* gQ,
+template <typename T, typename TO>
+cudaError_t grad_q_typed(const Problem& P, const float* g, const int32_t* am, TO* gQ,
                          cudaStream_t stream, unsigned int* err) {
     const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t blocks = P.n_query * groups;
     if (P.dim % kVec == 0 && P.dim <= 256 && blocks < (int64_t(1) << 31)) {
         // 8 (dim <= 128) or 4 (dim <= 256) independent row loads in flight per thread
         if (P.dim <= 128)
-            grad_q_vec_kernel<T, 2, 8><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+            grad_q_vec_kernel<T, 2, 8, TO><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
         else
-            grad_q_vec_kernel<T, 4, 4><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
+            grad_q_vec_kernel<T, 4, 4, TO><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(P, g, am, gQ, err);
         return cudaGetLastError();
     }
-    grad_q_gather_kernel<T><<<grid_for(P.n_query * P.Lq, 16), kThreads, 0, stream>>>(P, g, am, gQ, err);
+    grad_q_gather_kernel<T, TO><<<grid_for(P.n_query * P.Lq, 16), kThreads, 0, stream>>>(P, g, am, gQ, err);
     return cudaGetLastError();
 }
 
@@ -347,9 +690,9 @@ cudaError_t launch_bwd_grad_q(const Problem& P, const float* g, const int32_t* a
     if (P.n_query * P.Lq == 0) return cudaSuccess;
     unsigned int* err = device_error_word();
     switch (P.dtype) {
-    case kF32: return grad_q_typed<float>(P, g, am, gQ, stream, err);
-    case kF16: return grad_q_typed<__half>(P, g, am, gQ, stream, err);
-    default: return grad_q_typed<__nv_bfloat16>(P, g, am, gQ, stream, err);
+    case kF32: return grad_q_typed<float, float>(P, g, am, gQ, stream, err);
+    case kF16: return grad_q_typed<__half, float>(P, g, am, gQ, stream, err);
+    default: return grad_q_typed<__nv_bfloat16, float>(P, g, am, gQ, stream, err);
     }
 }
 
@@ -366,6 +709,68 @@ cudaError_t launch_bwd_grad_d(const Problem& P, const float* g, const int32_t* a
     case kF16: return grad_d_typed<__half>(P, g, am, gD, stream, err);
     default: return grad_d_typed<__nv_bfloat16>(P, g, am, gD, stream, err);
     }
+}
+
+
+namespace {
+
+template <typename T, typename TO>
+cudaError_t grad_d_same_typed(const Problem& P, const float* g, const int32_t* am, TO* gD, cudaStream_t stream,
+                              unsigned int* err) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int64_t sms = device_info(dev).sm_count;
+    if (P.layout != kAllPairs && P.Lq <= 32) {
+        const int64_t grid = P.n_doc < sms * 8 ? P.n_doc : sms * 8;
+        if (P.dim <= kOwnRowThreads * kVec)
+            grad_d_doc_stream_kernel<T, 1, TO><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(P, g, am, gD, err);
+        else
+            grad_d_doc_stream_kernel<T, 2, TO><<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(P, g, am, gD, err);
+        return cudaGetLastError();
+    }
+    if (P.layout == kAllPairs && P.n_query * P.Lq <= kOwnWindow) {
+        const int64_t chunks = (P.Ld + kOwnRows - 1) / kOwnRows;
+        const int64_t blocks = P.n_doc * chunks;
+        if (P.dim <= kOwnRowThreads * kVec)
+            grad_d_owner_kernel<T, 1, TO><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(P, g, am, gD, chunks, err);
+        else
+            grad_d_owner_kernel<T, 2, TO><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(P, g, am, gD, chunks, err);
+        return cudaGetLastError();
+    }
+    const int64_t rows_per_cta = kChunkFloats / P.dim;
+    const int64_t chunks = (P.Ld + rows_per_cta - 1) / rows_per_cta;
+    const int64_t blocks = P.n_doc * chunks;
+    const int smem = (kChunkFloats + kChunkRound) * static_cast<int>(sizeof(float));
+    cudaError_t e = cudaFuncSetAttribute(grad_d_chunk_kernel<T, TO>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    grad_d_chunk_kernel<T, TO><<<static_cast<unsigned>(blocks), kThreads, smem, stream>>>(P, g, am, gD, rows_per_cta,
+                                                                                          chunks, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool bwd_same_dtype_supported(const Problem& P) {
+    const int64_t chunks = P.dim > 0 ? (P.Ld + kChunkFloats / P.dim - 1) / (kChunkFloats / P.dim) : 0;
+    return (P.dtype == kF16 || P.dtype == kBF16) && P.dim % kVec == 0 && P.dim <= 2 * kOwnRowThreads * kVec &&
+           P.n_doc * chunks < (int64_t(1) << 31) && P.n_query * P.Lq < (int64_t(1) << 31) &&
+           P.n_pairs < (int64_t(1) << 31);
+}
+
+cudaError_t launch_bwd_grad_q_same(const Problem& P, const float* g, const int32_t* am, void* gQ,
+                                   cudaStream_t stream) {
+    if (P.n_query * P.Lq == 0) return cudaSuccess;
+    unsigned int* err = device_error_word();
+    if (P.dtype == kF16) return grad_q_typed<__half, __half>(P, g, am, static_cast<__half*>(gQ), stream, err);
+    return grad_q_typed<__nv_bfloat16, __nv_bfloat16>(P, g, am, static_cast<__nv_bfloat16*>(gQ), stream, err);
+}
+
+cudaError_t launch_bwd_grad_d_same(const Problem& P, const float* g, const int32_t* am, void* gD,
+                                   cudaStream_t stream) {
+    if (P.n_doc * P.Ld * P.dim == 0) return cudaSuccess;
+    unsigned int* err = device_error_word();
+    if (P.dtype == kF16) return grad_d_same_typed<__half, __half>(P, g, am, static_cast<__half*>(gD), stream, err);
+    return grad_d_same_typed<__nv_bfloat16, __nv_bfloat16>(P, g, am, static_cast<__nv_bfloat16*>(gD), stream, err);
 }
 
 }  // namespace lik

@@ -637,7 +637,12 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
     p.Ld = P.Ld;
     p.dim = static_cast<int>(P.dim);
     p.atoms = (p.dim + kAtomElems - 1) / kAtomElems;
-    const int tmax = p.atoms <= 2 ? kMaxTileCols : 128;
+    p.q_bytes = static_cast<uint32_t>(p.atoms * kM * kAtomBytes);
+    const size_t misc = sizeof(Bars) + sizeof(Exchange);
+    const size_t budget = static_cast<size_t>(info.max_smem_optin) - 1024 - misc - 2 * p.q_bytes;
+    // widest tile (<= 256 tokens) that leaves room for two D stages
+    int tmax = kMaxTileCols;
+    while (tmax > 16 && budget / (static_cast<size_t>(p.atoms) * tmax * kAtomBytes) < 2) tmax -= 16;
     p.tiles_per_doc = ceil_div(P.Ld, tmax);
     p.T = ((ceil_div(P.Ld, p.tiles_per_doc) + 15) / 16) * 16;
     // as many accumulator buffers as TMEM holds at a 32-column-aligned stride
@@ -647,10 +652,7 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
     p.acc_stride = (kTmemCols / p.nacc) / 32 * 32;
     p.qpt = static_cast<int>(kM / P.Lq);
     p.n_rb = ceil_div(P.n_query, p.qpt);
-    p.q_bytes = static_cast<uint32_t>(p.atoms * kM * kAtomBytes);
     p.d_bytes = static_cast<uint32_t>(p.atoms * p.T * kAtomBytes);
-    const size_t misc = sizeof(Bars) + sizeof(Exchange);
-    const size_t budget = static_cast<size_t>(info.max_smem_optin) - 1024 - misc - 2 * p.q_bytes;
     p.stages = static_cast<int>(budget / p.d_bytes);
     if (p.stages > kMaxStages) p.stages = kMaxStages;
     if (p.stages < 2) return cudaErrorInvalidConfiguration;

@@ -546,11 +546,28 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 
 }  // namespace
 
+// D stages the kernel's shared memory holds for this problem (at least two
+// are needed): the query rows (two buffers), the per-document dumps and the
+// barriers come first.
+int stream_stages(const Problem& P, int max_smem_optin) {
+    const int atoms = static_cast<int>((P.dim + kAtomElems - 1) / kAtomElems);
+    const int groups = static_cast<int>((P.Lq + 31) / 32);
+    const size_t q_bytes = static_cast<size_t>(atoms) * 32 * groups * kAtomBytes;
+    const size_t d_bytes = static_cast<size_t>(atoms) * kRows * kAtomBytes;
+    const size_t misc = sizeof(Bars) + sizeof(Shared) + 2 * static_cast<size_t>(groups) * sizeof(Dump);
+    const size_t need = 1024 + misc + 2 * q_bytes;
+    if (static_cast<size_t>(max_smem_optin) <= need) return 0;
+    const size_t stages = (static_cast<size_t>(max_smem_optin) - need) / d_bytes;
+    return stages > kMaxStages ? kMaxStages : static_cast<int>(stages);
+}
+
 bool tc_stream_eligible(const Problem& P) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
     return (P.layout == kPairwise || P.layout == kKd) && (P.dtype == kF16 || P.dtype == kBF16) &&
            P.dim % 16 == 0 && P.dim <= kMaxDim && P.Lq >= 1 && P.Lq <= 32 * kMaxGroups && P.Ld >= 1 &&
            P.n_query * P.Lq < (int64_t(1) << 31) && P.Ld < (int64_t(1) << 31) &&
-           P.n_doc < (int64_t(1) << 31);
+           P.n_doc < (int64_t(1) << 31) && stream_stages(P, device_info(dev).max_smem_optin) >= 2;
 }
 
 cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax, cudaStream_t stream) {
@@ -576,10 +593,8 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
     p.q_bytes = static_cast<uint32_t>(p.atoms * p.np * kAtomBytes);
     p.d_bytes = static_cast<uint32_t>(p.atoms * kRows * kAtomBytes);
     const size_t misc = sizeof(Bars) + sizeof(Shared) + 2 * static_cast<size_t>(p.groups) * sizeof(Dump);
-    const size_t budget = static_cast<size_t>(info.max_smem_optin) - 1024 - misc - 2 * p.q_bytes;
-    p.stages = static_cast<int>(budget / p.d_bytes);
-    if (p.stages > kMaxStages) p.stages = kMaxStages;
-    if (p.stages < 2) return cudaErrorInvalidConfiguration;
+    p.stages = stream_stages(P, info.max_smem_optin);
+    if (p.stages < 2) return cudaErrorInvalidConfiguration;  // tc_stream_eligible rules this out
     p.idesc = ptx::f16_idesc(kRows, p.np, P.dtype == kBF16);
     p.qmask = P.qmask;
     p.dmask = P.dmask;

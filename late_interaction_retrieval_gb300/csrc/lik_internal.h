@@ -86,4 +86,12 @@ cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,
 cudaError_t launch_bwd_grad_d(const Problem& P, const float* grad_out,
                               const int32_t* argmax, float* grad_D, cudaStream_t stream);
 
+// Backward with gradients in the inputs' 16-bit dtype: fp32 sums, one rounded
+// write per element, no zero-fill.  fp16/bf16, dim % 8 == 0, dim <= 256.
+bool bwd_same_dtype_supported(const Problem& P);
+cudaError_t launch_bwd_grad_q_same(const Problem& P, const float* grad_out, const int32_t* argmax,
+                                   void* grad_Q, cudaStream_t stream);
+cudaError_t launch_bwd_grad_d_same(const Problem& P, const float* grad_out, const int32_t* argmax,
+                                   void* grad_D, cudaStream_t stream);
+
 }  // namespace lik

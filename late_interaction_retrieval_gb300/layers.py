@@ -10,9 +10,11 @@ for late-interaction-kernels (LIK)" (Design section):
 
 Masks are bool, True = valid, or None.  Scores are fp32.  The forward saves
 only the int32 argmax [pairs, Lq] (linear in the number of pairs; no
-[pairs, Lq, Ld] similarity grid exists anywhere).  The backward asks liblik
-for fp32 gradients and casts them to the input dtype.  This module only
-allocates tensors and calls the binding.
+[pairs, Lq, Ld] similarity grid exists anywhere).  For fp16/bf16 inputs with
+dim % 8 == 0 and dim <= 256 the backward asks liblik for gradients in the
+input dtype directly (summed in fp32, rounded once); otherwise it asks for
+fp32 gradients and casts them.  This module only allocates tensors and calls
+the binding.
 """
 from __future__ import annotations
 
@@ -23,6 +25,18 @@ from . import binding
 
 def _contig(t):
     return None if t is None else t.contiguous()
+
+
+def _backward(kind, ctx, g):
+    """Gradients of Q and D for layout `kind` from the saved argmax."""
+    Q, D, argmax = ctx.saved_tensors
+    same = Q.dtype != torch.float32 and Q.shape[-1] % 8 == 0 and Q.shape[-1] <= 256
+    gdt = Q.dtype if same else torch.float32
+    gQ = torch.empty(Q.shape, dtype=gdt, device=Q.device) if ctx.needs_input_grad[0] else None
+    gD = torch.empty(D.shape, dtype=gdt, device=D.device) if ctx.needs_input_grad[1] else None
+    fn = getattr(binding, f"lik_maxsim_{kind}_bwd" + ("_same_dtype" if same else ""))
+    fn(Q, D, g.contiguous().float(), argmax, gQ, gD)
+    return (None if gQ is None else gQ.to(Q.dtype), None if gD is None else gD.to(D.dtype), None, None)
 
 
 class _MaxSimFn(torch.autograd.Function):
@@ -40,12 +54,7 @@ class _MaxSimFn(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, g):
-        Q, D, argmax = ctx.saved_tensors
-        gQ = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if ctx.needs_input_grad[0] else None
-        gD = torch.empty(D.shape, dtype=torch.float32, device=D.device) if ctx.needs_input_grad[1] else None
-        binding.lik_maxsim_allpairs_bwd(Q, D, g.contiguous().float(), argmax, gQ, gD)
-        return (None if gQ is None else gQ.to(Q.dtype), None if gD is None else gD.to(D.dtype),
-                None, None)
+        return _backward("allpairs", ctx, g)
 
 
 class _MaxSimPairwiseFn(torch.autograd.Function):
@@ -62,12 +71,7 @@ class _MaxSimPairwiseFn(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, g):
-        Q, D, argmax = ctx.saved_tensors
-        gQ = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if ctx.needs_input_grad[0] else None
-        gD = torch.empty(D.shape, dtype=torch.float32, device=D.device) if ctx.needs_input_grad[1] else None
-        binding.lik_maxsim_pairwise_bwd(Q, D, g.contiguous().float(), argmax, gQ, gD)
-        return (None if gQ is None else gQ.to(Q.dtype), None if gD is None else gD.to(D.dtype),
-                None, None)
+        return _backward("pairwise", ctx, g)
 
 
 class _MaxSimKDFn(torch.autograd.Function):
@@ -85,12 +89,7 @@ class _MaxSimKDFn(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, g):
-        Q, D, argmax = ctx.saved_tensors
-        gQ = torch.empty(Q.shape, dtype=torch.float32, device=Q.device) if ctx.needs_input_grad[0] else None
-        gD = torch.empty(D.shape, dtype=torch.float32, device=D.device) if ctx.needs_input_grad[1] else None
-        binding.lik_maxsim_kd_bwd(Q, D, g.contiguous().float(), argmax, gQ, gD)
-        return (None if gQ is None else gQ.to(Q.dtype), None if gD is None else gD.to(D.dtype),
-                None, None)
+        return _backward("kd", ctx, g)
 
 
 def maxsim(Q, D, qmask=None, dmask=None):

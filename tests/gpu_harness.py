@@ -85,6 +85,21 @@ class Layout:
         binding.lik_check_device_error()
         return gQ.cpu().numpy(), gD.cpu().numpy()
 
+    def gpu_bwd_same_dtype(self, grad_out, argmax, device="cuda"):
+        """Gradients from the entry points that write them in the inputs' dtype
+        (outputs start as NaN, so an element the kernels skip shows up)."""
+        Q, D, _, _ = self.gpu_inputs(device)
+        g = torch.as_tensor(np.ascontiguousarray(grad_out), dtype=torch.float32).to(device)
+        am = torch.as_tensor(np.ascontiguousarray(argmax), dtype=torch.int32).to(device)
+        shape = self.inp.workload.score_shape
+        g = g.reshape(shape)
+        am = am.reshape(*shape, self.Lq)
+        gQ = torch.full(Q.shape, float("nan"), dtype=Q.dtype, device=device)
+        gD = torch.full(D.shape, float("nan"), dtype=D.dtype, device=device)
+        getattr(binding, f"lik_maxsim_{self.kind}_bwd_same_dtype")(Q, D, g, am, gQ, gD)
+        binding.lik_check_device_error()
+        return gQ.float().cpu().numpy(), gD.float().cpu().numpy()
+
     # ---- comparisons ------------------------------------------------------
     def check_forward(self):
         s_o, am_o, gap = self.oracle_fwd()
@@ -116,3 +131,19 @@ class Layout:
         eq = parity.assert_grad_close(gQ_g, gQ_o, tag, "grad_Q")
         ed = parity.assert_grad_close(gD_g, gD_o, tag, "grad_D")
         return dict(grad_q_err=eq, grad_d_err=ed)
+
+    def check_backward_same_dtype(self, am_oracle):
+        """Same-dtype gradients against the oracle: the bar plus one rounding to
+        the output type (2^-8 relative for bf16, 2^-11 for fp16)."""
+        g32 = np.asarray(self.inp.grad_out.cpu().numpy(), np.float32).astype(np.float64)
+        gQ_o, gD_o = self.oracle_bwd(g32, am_oracle)
+        gQ_g, gD_g = self.gpu_bwd_same_dtype(g32, am_oracle)
+        tag = self.inp.workload.dtype
+        tol = parity.TOL[tag] + {"bf16": 2.0 ** -8, "f16": 2.0 ** -11, "f32": 0.0}[tag]
+        out = {}
+        for got, ref, name in ((gQ_g, gQ_o, "grad_Q"), (gD_g, gD_o, "grad_D")):
+            assert np.isfinite(got).all(), f"{name}: an element was not written"
+            err = parity.normwise_rel_err(got, ref)
+            assert err <= tol, f"{name}: normwise relative error {err:.3g} > {tol:.3g}"
+            out[name] = err
+        return out

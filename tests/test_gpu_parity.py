@@ -76,6 +76,8 @@ SWEEP = [
     ("allpairs",   2,  3, 128, 300,  128),
     ("allpairs",  17,  3,  8,   64,   64),
     ("allpairs",   3,  6, 100,  33,  256),
+    ("allpairs",   3,  4, 32,  300,  256),  # 80-column tiles: the widest with two D stages at dim 256
+    ("kd",         2,  3, 16,  150,  256),  # streaming forward does not fit at dim 256: SIMT forward
     ("allpairs",   2,  2,  7,   31,   16),
     ("allpairs",   2,  3,  5,   40,   96),
     ("allpairs",   4, 400, 32, 300,  128),  # 160-column tiles, 3 accumulators, several per CTA
