@@ -64,6 +64,8 @@ def _declare(lib):
     lib.oracle_pairwise_bwd.argtypes = fwd_common + [i64] * 4 + [ptr] * 4
     lib.oracle_kd_bwd.restype = None
     lib.oracle_kd_bwd.argtypes = fwd_common + [i64] * 5 + [ptr] * 4
+    lib.oracle_ce_rows.restype = None
+    lib.oracle_ce_rows.argtypes = [ptr, i64, i64, ptr, dbl, ptr, ptr, ptr]
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_set_num_threads.restype = None
@@ -227,6 +229,18 @@ class Oracle:
         self.lib.oracle_kd_bwd(_c(Q), _c(D), code, B, N, Lq, Ld, dim,
                                _c(g), _c(am), _c(gQ), _c(gD))
         return gQ, gD
+
+
+    def ce_rows(self, scores, target, scale=1.0):
+        """Mean softmax cross-entropy over score rows: (loss, row_loss, grad)."""
+        S = np.ascontiguousarray(scores, dtype=np.float64)
+        rows, cols = S.shape
+        t = np.ascontiguousarray(target, dtype=np.int32).reshape(rows)
+        row_loss = np.empty(rows, np.float64)
+        grad = np.empty((rows, cols), np.float64)
+        loss = np.empty(1, np.float64)
+        self.lib.oracle_ce_rows(_c(S), rows, cols, _c(t), float(scale), _c(row_loss), _c(grad), _c(loss))
+        return float(loss[0]), row_loss, grad
 
 
 _default = None

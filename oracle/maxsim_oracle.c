@@ -316,6 +316,48 @@ void oracle_kd_bwd(const void* Q, const void* D, int dtype,
     free(di);
 }
 
+/*
+ * Cross-entropy head over score rows (colpali PR "Add support for
+ * late-interaction-kernels (LIK)", "What this PR adds": the in-batch ColBERT
+ * losses score a query against the batch's documents with its own document
+ * as the target, the negative-document losses score it against its own
+ * candidates with the positive first; "Results": the benchmarks time that
+ * head, forward and backward).  For every row r of scores[rows, cols] with
+ * logits z = scale * scores[r, :] and target t = target[r]:
+ *     row_loss[r] = log(sum over c of exp(z_c)) - z_t
+ *     grad[r, c]  = scale * (exp(z_c) / sum exp(z) - [c == t]) / rows
+ * and loss = (sum over r of row_loss[r]) / rows, i.e. the mean cross-entropy
+ * and its gradient with respect to the scores.  The log-sum-exp subtracts
+ * the row max first; everything is fp64.  A row whose target is outside
+ * [0, cols) gets row_loss 0 and a zero gradient and still counts in the mean.
+ */
+void oracle_ce_rows(const double* scores, int64_t rows, int64_t cols, const int32_t* target,
+                    double scale, double* row_loss, double* grad, double* loss)
+{
+    double total = 0.0;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* s = scores + r * cols;
+        double* gr = grad + r * cols;
+        const int32_t t = target[r];
+        if (t < 0 || t >= cols) {
+            row_loss[r] = 0.0;
+            for (int64_t c = 0; c < cols; ++c) gr[c] = 0.0;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t c = 0; c < cols; ++c)
+            if (scale * s[c] > m) m = scale * s[c];
+        double sum = 0.0;
+        for (int64_t c = 0; c < cols; ++c) sum += exp(scale * s[c] - m);
+        const double lse = m + log(sum);
+        row_loss[r] = lse - scale * s[t];
+        for (int64_t c = 0; c < cols; ++c)
+            gr[c] = scale * (exp(scale * s[c] - lse) - (c == t ? 1.0 : 0.0)) / (double)rows;
+        total += row_loss[r];
+    }
+    *loss = rows > 0 ? total / (double)rows : 0.0;
+}
+
 /* Number of threads the OpenMP loops above use. */
 int oracle_num_threads(void)
 {

@@ -314,6 +314,63 @@ def check_finite_difference_gradients(orc):
         np.testing.assert_allclose(G, num, rtol=1e-6, atol=1e-7)
 
 
+# ---------------------------------------------------- cross-entropy head --
+
+def check_ce_golden(orc):
+    """The hand-worked cases of tests/golden/ce_hand_worked.json."""
+    with open(os.path.join(os.path.dirname(__file__), "golden", "ce_hand_worked.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        loss, row_loss, grad = orc.ce_rows(np.array(c["scores"]), np.array(c["target"]), c["scale"])
+        np.testing.assert_allclose(loss, c["loss"], rtol=1e-14, atol=1e-15, err_msg=c["name"])
+        np.testing.assert_allclose(row_loss, c["row_loss"], rtol=1e-14, atol=1e-15, err_msg=c["name"])
+        np.testing.assert_allclose(grad, c["grad"], rtol=1e-14, atol=1e-15, err_msg=c["name"])
+
+
+def check_ce_invariants(orc):
+    """Shift invariance per row, gradient rows summing to zero with the only
+    negative entry at the target, the scale acting on the logits, and equal
+    logits giving log(cols)."""
+    rng = np.random.default_rng(21)
+    S = rng.standard_normal((6, 9)) * 3
+    t = rng.integers(0, 9, size=6)
+    loss, rl, g = orc.ce_rows(S, t)
+    loss2, rl2, g2 = orc.ce_rows(S + rng.standard_normal((6, 1)) * 50, t)
+    np.testing.assert_allclose(rl2, rl, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g2, g, rtol=1e-9, atol=1e-13)
+    np.testing.assert_allclose(g.sum(axis=1), 0.0, atol=1e-15)
+    for r in range(6):
+        assert g[r, t[r]] < 0 and np.all(np.delete(g[r], t[r]) > 0)
+    assert np.isclose(loss, rl.mean(), rtol=1e-15)
+    # scale 2 on S is scale 1 on 2S for the loss; the gradient picks up the factor
+    l3, rl3, g3 = orc.ce_rows(S, t, 2.0)
+    l4, rl4, g4 = orc.ce_rows(2 * S, t, 1.0)
+    np.testing.assert_allclose(rl3, rl4, rtol=1e-13)
+    np.testing.assert_allclose(g3, 2 * g4, rtol=1e-12, atol=1e-15)
+    # equal logits
+    l5, rl5, g5 = orc.ce_rows(np.full((3, 7), 0.25), np.array([0, 3, 6]))
+    np.testing.assert_allclose(rl5, np.log(7.0), rtol=1e-15)
+
+
+def check_ce_finite_difference(orc):
+    """Central differences of the mean loss with respect to every score."""
+    rng = np.random.default_rng(22)
+    S = rng.standard_normal((4, 5))
+    t = np.array([0, 4, 2, 1])
+    _, _, g = orc.ce_rows(S, t, 1.7)
+    h = 1e-6
+    num = np.zeros_like(S)
+    for idx in np.ndindex(S.shape):
+        old = S[idx]
+        S[idx] = old + h
+        fp = orc.ce_rows(S, t, 1.7)[0]
+        S[idx] = old - h
+        fm = orc.ce_rows(S, t, 1.7)[0]
+        S[idx] = old
+        num[idx] = (fp - fm) / (2 * h)
+    np.testing.assert_allclose(g, num, rtol=1e-7, atol=1e-9)
+
+
 ALL_CHECKS = [
     check_golden_cases,
     check_naive_reference,
@@ -327,4 +384,7 @@ ALL_CHECKS = [
     check_closed_form_unit_copies,
     check_degenerate_lengths,
     check_finite_difference_gradients,
+    check_ce_golden,
+    check_ce_invariants,
+    check_ce_finite_difference,
 ]

@@ -30,6 +30,11 @@ MUTANTS = [
     ("bf16_shift", "(uint32_t)h << 16", "(uint32_t)h << 15"),
     ("f16_bias", "e - 25", "e - 24"),
     ("f16_subnormal_scale", "ldexp((double)m, -24)", "ldexp((double)m, -25)"),
+    ("ce_loss_not_mean", "*loss = rows > 0 ? total / (double)rows : 0.0;", "*loss = total;"),
+    ("ce_grad_no_onehot", "(c == t ? 1.0 : 0.0)", "(c == t ? 0.0 : 0.0)"),
+    ("ce_grad_no_scale", "gr[c] = scale * (exp", "gr[c] = (exp"),
+    ("ce_wrong_target_logit", "row_loss[r] = lse - scale * s[t];", "row_loss[r] = lse - scale * s[0];"),
+    ("ce_grad_not_mean", "/ (double)rows;", ";"),
     ("kd_wrong_candidate", "score_blocks(Q, D, dtype, b, p, Lq", "score_blocks(Q, D, dtype, b, b, Lq"),
     ("pairwise_wrong_doc", "scores[b] = score_blocks(Q, D, dtype, b, b,",
      "scores[b] = score_blocks(Q, D, dtype, b, (b + 1) % B,"),
