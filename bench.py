@@ -176,7 +176,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the liblik calls of one step of a workload."""
 
-    def __init__(self, name: str, device: torch.device, grad_dtype: str = "f32"):
+    def __init__(self, name: str, device: torch.device, grad_dtype: str = "f32", ce: bool = False):
         from late_interaction_retrieval_gb300 import binding
         self.binding = binding
         self.w = W.WORKLOADS[name]
@@ -192,9 +192,20 @@ class Step:
         gdt = i.Q.dtype if self.same_dtype else torch.float32
         self.gQ = torch.empty(i.Q.shape, dtype=gdt, device=device) if w.backward else None
         self.gD = torch.empty(i.D.shape, dtype=gdt, device=device) if w.backward else None
+        # ce: the workload's cross-entropy head (loss and score gradient) runs
+        # inside every step, through lik_ce_rows, instead of once outside
+        self.ce = ce and w.backward and i.ce_target is not None
+        if ce and not self.ce:
+            raise SystemExit(f"--step ce: workload {name} has no cross-entropy head")
+        if self.ce:
+            self.target = i.ce_target.to(device=device, dtype=torch.int32).contiguous()
+            self.loss = torch.empty(1, dtype=torch.float32, device=device)
+            self.row_loss = torch.empty(w.nq, dtype=torch.float32, device=device)
         self.fwd()
         torch.cuda.synchronize()
-        if w.backward:
+        if self.ce:
+            self.g = torch.empty(w.score_shape, dtype=torch.float32, device=device)
+        elif w.backward:
             if i.grad_out is not None:
                 self.g = i.grad_out.to(device).float().contiguous()
             else:  # cross-entropy head of the workload: computed once, outside the timed steps
@@ -211,14 +222,18 @@ class Step:
 
     def bwd(self, Q=None, D=None, g=None):
         i = self.inp
+        if self.ce:
+            self.binding.lik_ce_rows(self.scores.view(self.w.nq, -1), self.target, self.loss, self.row_loss,
+                                     self.g.view(self.w.nq, -1))
         getattr(self.binding, f"lik_maxsim_{self.layout}_bwd" + ("_same_dtype" if self.same_dtype else ""))(
             i.Q if Q is None else Q, i.D if D is None else D, self.g if g is None else g,
             self.argmax, self.gQ, self.gD)
 
-    # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours)
+    # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours;
+    # the cross-entropy head is two kernels: per-row terms, then their mean)
     @property
     def launches_per_step(self) -> int:
-        return 1 + (2 if self.w.backward else 0)
+        return 1 + (2 if self.w.backward else 0) + (2 if self.ce else 0)
 
     def valid_flops(self) -> int:
         i, w = self.inp, self.w
@@ -254,7 +269,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     name = args.workload
-    st = Step(name, device, args.grad_dtype)
+    st = Step(name, device, args.grad_dtype, ce=args.step == "ce")
     w = st.w
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -344,6 +359,7 @@ def run_ours(args):
                 "workload": name, "layout": w.layout,
                 "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
                 "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
+                "loss_head": "cross-entropy inside the step" if st.ce else "score gradient precomputed",
                 "counted_flops_per_step": counted, "valid_token_flops_per_step": st.valid_flops(),
                 "algorithmic_fwd_bytes": st.algorithmic_bytes(),
                 "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -368,10 +384,15 @@ def run_e2e(st: Step, args, stream, world):
     i, w = st.inp, st.w
     host = {k: v.cpu().pin_memory() for k, v in
             (("Q", i.Q), ("D", i.D), ("qm", i.qmask), ("dm", i.dmask))}
-    if w.backward:
+    if st.ce:
+        host["target"] = st.target.cpu().pin_memory()
+    elif w.backward:
         host["g"] = st.g.cpu().pin_memory()
     dev = {k: torch.empty_like(v, device=st.device) for k, v in host.items()}
-    outs = [st.scores] + ([st.gQ, st.gD] if w.backward else [])
+    if st.ce:  # the loss head in one call; the loss and both gradients come back
+        outs = [st.loss, st.gQ, st.gD]
+    else:
+        outs = [st.scores] + ([st.gQ, st.gD] if w.backward else [])
     back = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = sum(o.numel() * o.element_size() for o in outs)
@@ -379,9 +400,14 @@ def run_e2e(st: Step, args, stream, world):
     def step():
         for k in host:
             dev[k].copy_(host[k], non_blocking=True)
-        st.fwd(dev["Q"], dev["D"], dev["qm"], dev["dm"])
-        if w.backward:
-            st.bwd(dev["Q"], dev["D"], dev["g"])
+        if st.ce:
+            getattr(st.binding, f"lik_maxsim_{w.layout}_ce_step")(
+                dev["Q"], dev["D"], dev["qm"], dev["dm"], dev["target"], st.scores, st.argmax, st.loss,
+                st.row_loss, st.g, st.gQ, st.gD)
+        else:
+            st.fwd(dev["Q"], dev["D"], dev["qm"], dev["dm"])
+            if w.backward:
+                st.bwd(dev["Q"], dev["D"], dev["g"])
         for o, b in zip(outs, back):
             b.copy_(o, non_blocking=True)
 
@@ -519,6 +545,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="inbatch_b128_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", choices=["fwd+bwd", "ce"], default="fwd+bwd",
+                    help="ce: the workload's cross-entropy head (loss and score gradient) inside every step")
     ap.add_argument("--grad-dtype", choices=["f32", "input"], default="f32",
                     help="gradients in fp32 (default) or in the inputs' dtype (the _bwd_same_dtype entry points)")
     args = ap.parse_args()

@@ -203,6 +203,55 @@ lik_status lik_maxsim_kd_bwd_same_dtype(const void* Q, const void* D, lik_dtype 
                                         const float* grad_out, const int32_t* argmax,
                                         void* grad_Q, void* grad_D, cudaStream_t stream);
 
+/* --------------------------------------------------- cross-entropy head --
+ * colpali PR "Add support for late-interaction-kernels (LIK)": "What this PR
+ * adds" routes the in-batch ColBERT losses (a query against the batch's
+ * documents, its own document the target) and the negative-document losses
+ * (a query against its own candidates, the positive first, via the kd
+ * layout) through the kernel; "Results" time that loss head forward and
+ * backward.
+ *
+ * lik_ce_rows: softmax cross-entropy over the rows of scores[rows, cols]
+ * with logits z = scale * scores[r, :] and target[r]:
+ *     row_loss[r]       = log(sum_c exp(z_c)) - z_target         (fp32, written)
+ *     *loss             = mean over rows of row_loss             (fp32, written)
+ *     grad_scores[r, c] = scale * (softmax(z)_c - [c == target]) / rows
+ *                         (the gradient of *loss; written unless NULL)
+ * A target outside [0, cols) leaves its row out (row_loss 0, zero gradient);
+ * the mean still divides by rows.  Rows of -1e9 (empty documents) add
+ * nothing to the softmax.  The mean is summed in a fixed order.
+ *   scores [rows, cols], target [rows] int32, loss [1], row_loss [rows]:
+ *   device pointers, 4-byte aligned; all but grad_scores required.
+ */
+lik_status lik_ce_rows(const float* scores, int64_t rows, int64_t cols, const int32_t* target,
+                       float scale, float* loss, float* row_loss, float* grad_scores,
+                       cudaStream_t stream);
+
+/*
+ * One loss-head training step on `stream`, with no host synchronisation:
+ * the forward (scores and argmax), lik_ce_rows over the score rows
+ * (all-pairs: rows = Nq, cols = Nd; kd: rows = B, cols = N), then the
+ * backward with grad_out = grad_scores.  Gradients are fp32 (grad_Q, grad_D
+ * as float*) or, with grads_in_input_dtype != 0, in the inputs' dtype as in
+ * the _bwd_same_dtype entry points.  Arguments, shapes and errors as in the
+ * entry points it calls; scores, argmax, loss, row_loss and grad_scores are
+ * caller-allocated outputs.  It returns the first non-OK status.
+ */
+lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
+                                       int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,
+                                       const bool* qmask, const bool* dmask,
+                                       const int32_t* target, float scale, float* scores,
+                                       int32_t* argmax, float* loss, float* row_loss,
+                                       float* grad_scores, void* grad_Q, void* grad_D,
+                                       int grads_in_input_dtype, cudaStream_t stream);
+
+lik_status lik_maxsim_kd_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                                 int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                 const bool* dmask, const int32_t* target, float scale,
+                                 float* scores, int32_t* argmax, float* loss, float* row_loss,
+                                 float* grad_scores, void* grad_Q, void* grad_D,
+                                 int grads_in_input_dtype, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -37,6 +37,11 @@ SIGNATURES = {
     "lik_maxsim_allpairs_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_pairwise_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
     "lik_maxsim_kd_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_ce_rows": (_I32, [_P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
+    "lik_maxsim_allpairs_ce_step": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 3 + [ctypes.c_float]
+                                    + [_P] * 7 + [_I32, _P]),
+    "lik_maxsim_kd_ce_step": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 3 + [ctypes.c_float]
+                              + [_P] * 7 + [_I32, _P]),
 }
 
 _DTYPES = {torch.float32: LIK_F32, torch.float16: LIK_F16, torch.bfloat16: LIK_BF16}
@@ -255,6 +260,70 @@ def lik_maxsim_kd_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=Non
     _check(load().lik_maxsim_kd_bwd_same_dtype(
         _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
         _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+# --------------------------------------------------- cross-entropy head --
+
+def lik_ce_rows(scores, target, loss, row_loss, grad_scores=None, scale=1.0, stream=None):
+    """Mean softmax cross-entropy over the rows of scores [rows, cols]."""
+    if scores.dim() != 2:
+        raise ValueError("scores must be [rows, cols]")
+    dev = scores.device
+    rows, cols = scores.shape
+    _need(scores, "scores", (rows, cols), torch.float32, dev)
+    _need(target, "target", (rows,), torch.int32, dev)
+    _need(loss, "loss", (1,), torch.float32, dev)
+    _need(row_loss, "row_loss", (rows,), torch.float32, dev)
+    _need(grad_scores, "grad_scores", (rows, cols), torch.float32, dev, optional=True)
+    _check(load().lik_ce_rows(_ptr(scores), rows, cols, _ptr(target), float(scale), _ptr(loss),
+                              _ptr(row_loss), _ptr(grad_scores), _stream(dev, stream)))
+
+
+def _ce_step(kind, Q, D, qmask, dmask, target, scale, scores, argmax, loss, row_loss, grad_scores,
+             grad_Q, grad_D, stream):
+    if kind == "allpairs":
+        dt, dev = _embeddings(Q, D, 3, 3)
+        Nq, Lq, dim = Q.shape
+        Nd, Ld, _ = D.shape
+        sizes, rows, cols = (Nq, Nd, Lq, Ld, dim), Nq, Nd
+        dshape = (Nd, Ld)
+    else:
+        dt, dev = _embeddings(Q, D, 3, 4)
+        B, Lq, dim = Q.shape
+        N, Ld = D.shape[1], D.shape[2]
+        sizes, rows, cols = (B, N, Lq, Ld, dim), B, N
+        dshape = (B, N, Ld)
+    same = grad_Q is not None and grad_Q.dtype != torch.float32 or grad_D is not None and grad_D.dtype != torch.float32
+    gdt = Q.dtype if same else torch.float32
+    _need(qmask, "qmask", (Q.shape[0], Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", dshape, torch.bool, dev, optional=True)
+    _need(target, "target", (rows,), torch.int32, dev)
+    _need(scores, "scores", (rows, cols), torch.float32, dev)
+    _need(argmax, "argmax", (rows, cols, Lq), torch.int32, dev)
+    _need(loss, "loss", (1,), torch.float32, dev)
+    _need(row_loss, "row_loss", (rows,), torch.float32, dev)
+    _need(grad_scores, "grad_scores", (rows, cols), torch.float32, dev)
+    _need(grad_Q, "grad_Q", tuple(Q.shape), gdt, dev, optional=True)
+    _need(grad_D, "grad_D", tuple(D.shape), gdt, dev, optional=True)
+    _check(getattr(load(), f"lik_maxsim_{kind}_ce_step")(
+        _ptr(Q), _ptr(D), dt, *sizes, _ptr(qmask), _ptr(dmask), _ptr(target), float(scale),
+        _ptr(scores), _ptr(argmax), _ptr(loss), _ptr(row_loss), _ptr(grad_scores),
+        _ptr(grad_Q), _ptr(grad_D), 1 if same else 0, _stream(dev, stream)))
+
+
+def lik_maxsim_allpairs_ce_step(Q, D, qmask, dmask, target, scores, argmax, loss, row_loss, grad_scores,
+                                grad_Q=None, grad_D=None, scale=1.0, stream=None):
+    """In-batch cross-entropy head in one call: forward, loss, backward.
+    Gradients in fp32, or in the inputs' dtype when grad_Q/grad_D have it."""
+    _ce_step("allpairs", Q, D, qmask, dmask, target, scale, scores, argmax, loss, row_loss,
+             grad_scores, grad_Q, grad_D, stream)
+
+
+def lik_maxsim_kd_ce_step(Q, D, qmask, dmask, target, scores, argmax, loss, row_loss, grad_scores,
+                          grad_Q=None, grad_D=None, scale=1.0, stream=None):
+    """Per-query-candidate cross-entropy head in one call: forward, loss, backward."""
+    _ce_step("kd", Q, D, qmask, dmask, target, scale, scores, argmax, loss, row_loss,
+             grad_scores, grad_Q, grad_D, stream)
 
 
 def lik_check_device_error(stream=None, device=None):

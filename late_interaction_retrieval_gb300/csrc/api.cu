@@ -451,4 +451,65 @@ lik_status lik_maxsim_kd_bwd_same_dtype(const void* Q, const void* D, lik_dtype 
     return run_bwd_same(P, grad_out, argmax, grad_Q, grad_D, stream);
 }
 
+lik_status lik_ce_rows(const float* scores, int64_t rows, int64_t cols, const int32_t* target, float scale,
+                       float* loss, float* row_loss, float* grad_scores, cudaStream_t stream) {
+    t_message[0] = 0;
+    if (rows < 0 || cols < 0) return fail(LIK_ERR_INVALID_ARG, "negative size");
+    int dev = 0;
+    lik_status st = check_device(&dev);
+    if (st != LIK_OK) return st;
+    const Spec specs[] = {
+        {"scores", scores, true, rows * cols},
+        {"target", target, true, rows},
+        {"loss", loss, true, 1},
+        {"row_loss", row_loss, true, rows},
+        {"grad_scores", grad_scores, false, rows * cols},
+    };
+    if ((st = check_buffers(dev, specs, 5)) != LIK_OK) return st;
+    if ((st = check_aligned(scores, 4, "scores")) != LIK_OK) return st;
+    if ((st = check_aligned(target, 4, "target")) != LIK_OK) return st;
+    if ((st = check_aligned(loss, 4, "loss")) != LIK_OK) return st;
+    if ((st = check_aligned(row_loss, 4, "row_loss")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_scores, 4, "grad_scores")) != LIK_OK) return st;
+    const cudaError_t e = launch_ce_rows(scores, rows, cols, target, scale, loss, row_loss,
+                                         cols > 0 ? grad_scores : nullptr, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cross-entropy launch");
+    return LIK_OK;
+}
+
+lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t Nq, int64_t Nd,
+                                       int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                       const bool* dmask, const int32_t* target, float scale, float* scores,
+                                       int32_t* argmax, float* loss, float* row_loss, float* grad_scores,
+                                       void* grad_Q, void* grad_D, int grads_in_input_dtype,
+                                       cudaStream_t stream) {
+    lik_status st = lik_maxsim_allpairs_fwd(Q, D, dtype, Nq, Nd, Lq, Ld, dim, qmask, dmask, scores, argmax, stream);
+    if (st != LIK_OK) return st;
+    if (Nq > 0 && Nd > 0 && !grad_scores) return fail(LIK_ERR_INVALID_ARG, "grad_scores is NULL");
+    st = lik_ce_rows(scores, Nq, Nd, target, scale, loss, row_loss, grad_scores, stream);
+    if (st != LIK_OK) return st;
+    if (grads_in_input_dtype)
+        return lik_maxsim_allpairs_bwd_same_dtype(Q, D, dtype, Nq, Nd, Lq, Ld, dim, grad_scores, argmax, grad_Q,
+                                                  grad_D, stream);
+    return lik_maxsim_allpairs_bwd(Q, D, dtype, Nq, Nd, Lq, Ld, dim, grad_scores, argmax,
+                                   static_cast<float*>(grad_Q), static_cast<float*>(grad_D), stream);
+}
+
+lik_status lik_maxsim_kd_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N, int64_t Lq,
+                                 int64_t Ld, int64_t dim, const bool* qmask, const bool* dmask,
+                                 const int32_t* target, float scale, float* scores, int32_t* argmax, float* loss,
+                                 float* row_loss, float* grad_scores, void* grad_Q, void* grad_D,
+                                 int grads_in_input_dtype, cudaStream_t stream) {
+    lik_status st = lik_maxsim_kd_fwd(Q, D, dtype, B, N, Lq, Ld, dim, qmask, dmask, scores, argmax, stream);
+    if (st != LIK_OK) return st;
+    if (B > 0 && N > 0 && !grad_scores) return fail(LIK_ERR_INVALID_ARG, "grad_scores is NULL");
+    st = lik_ce_rows(scores, B, N, target, scale, loss, row_loss, grad_scores, stream);
+    if (st != LIK_OK) return st;
+    if (grads_in_input_dtype)
+        return lik_maxsim_kd_bwd_same_dtype(Q, D, dtype, B, N, Lq, Ld, dim, grad_scores, argmax, grad_Q, grad_D,
+                                            stream);
+    return lik_maxsim_kd_bwd(Q, D, dtype, B, N, Lq, Ld, dim, grad_scores, argmax, static_cast<float*>(grad_Q),
+                             static_cast<float*>(grad_D), stream);
+}
+
 }  // extern "C"

@@ -94,4 +94,9 @@ cudaError_t launch_bwd_grad_q_same(const Problem& P, const float* grad_out, cons
 cudaError_t launch_bwd_grad_d_same(const Problem& P, const float* grad_out, const int32_t* argmax,
                                    void* grad_D, cudaStream_t stream);
 
+// Softmax cross-entropy over score rows: per-row losses, their mean and the
+// gradient with respect to the scores (grad may be NULL).
+cudaError_t launch_ce_rows(const float* scores, int64_t rows, int64_t cols, const int32_t* target, float scale,
+                           float* loss, float* row_loss, float* grad, cudaStream_t stream);
+
 }  // namespace lik

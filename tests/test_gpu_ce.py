@@ -1,0 +1,98 @@
+"""Cross-entropy loss head (GPU) against the fp64 oracle.
+
+lik_ce_rows computes the mean softmax cross-entropy over score rows in fp32;
+its scores are given to both sides, so the fp32 bar (1e-5) applies.  The
+one-call steps (forward, loss, backward) start from embeddings: their scores
+carry the input dtype's error, so the loss and the score gradient are held to
+the fp16/bf16 bar, and Q/D gradients to the backward's bar where the GPU
+picked the oracle's argmax (as in the autograd test).
+"""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness
+import oracle
+import parity
+from late_interaction_retrieval_gb300 import binding
+from late_interaction_retrieval_gb300.workloads import random_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _ce_gpu(S, t, scale, with_grad=True):
+    dev = "cuda"
+    s = torch.as_tensor(S, dtype=torch.float32, device=dev).contiguous()
+    tt = torch.as_tensor(t, dtype=torch.int32, device=dev).contiguous()
+    loss = torch.full((1,), float("nan"), device=dev)
+    rl = torch.full((S.shape[0],), float("nan"), device=dev)
+    g = torch.full(S.shape, float("nan"), device=dev) if with_grad else None
+    binding.lik_ce_rows(s, tt, loss, rl, g, scale=scale)
+    torch.cuda.synchronize()
+    return loss.item(), rl.cpu().numpy(), None if g is None else g.cpu().numpy()
+
+
+@pytest.mark.parametrize("rows,cols,scale", [(5, 7, 1.0), (128, 128, 1.0), (256, 17, 2.5), (3, 4096, 0.7),
+                                             (1, 1, 1.0)])
+def test_ce_rows_matches_oracle(rows, cols, scale):
+    rng = np.random.default_rng(rows * 1000 + cols)
+    S = (rng.standard_normal((rows, cols)) * 4).astype(np.float32)
+    if cols > 2:
+        S[rng.random((rows, cols)) < 0.1] = -1e9  # empty documents
+    t = rng.integers(0, cols, size=rows).astype(np.int32)
+    if rows > 2:
+        t[1] = cols + 3  # a row left out
+    loss_o, rl_o, g_o = oracle.get().ce_rows(S.astype(np.float64), t, scale)
+    loss_g, rl_g, g_g = _ce_gpu(S, t, scale)
+    assert abs(loss_g - loss_o) <= 1e-5 * max(abs(loss_o), 1.0)
+    assert parity.normwise_rel_err(rl_g, rl_o) <= 1e-5
+    assert parity.normwise_rel_err(g_g, g_o) <= 1e-5
+    # the mean is summed in a fixed order
+    assert _ce_gpu(S, t, scale)[0] == loss_g
+
+
+def test_ce_rows_without_gradient_and_empty():
+    S = np.zeros((0, 4), np.float32)
+    loss, rl, _ = _ce_gpu(S, np.zeros(0, np.int32), 1.0, with_grad=False)
+    assert loss == 0.0 and rl.shape == (0,)
+    S = np.array([[0.5, 0.5]], np.float32)
+    loss, rl, _ = _ce_gpu(S, np.array([1], np.int32), 1.0, with_grad=False)
+    assert abs(loss - np.log(2)) < 1e-6
+
+
+@pytest.mark.parametrize("grads", ["f32", "input"])
+@pytest.mark.parametrize("layout,nq,nd,lq,ld,dim", [("allpairs", 6, 6, 32, 180, 128), ("allpairs", 9, 9, 16, 300, 64),
+                                                    ("kd", 4, 5, 32, 200, 128)])
+def test_ce_step_matches_oracle(layout, nq, nd, lq, ld, dim, grads):
+    inp = random_case(layout, nq, nd, lq, ld, dim, "bf16", seed=nq * 7 + nd, p_doc_empty=0.0)
+    h = gpu_harness.Layout(inp)
+    rows, cols = (nq, nd)
+    target = np.arange(rows, dtype=np.int32) % cols if layout == "allpairs" else np.zeros(rows, np.int32)
+    # oracle: forward, loss, backward on its own scores and argmax
+    s_o, am_o, _ = h.oracle_fwd()
+    scale = 1.5
+    loss_o, rl_o, gs_o = oracle.get().ce_rows(s_o.reshape(rows, cols), target, scale)
+    gQ_o, gD_o = h.oracle_bwd(gs_o.reshape(-1), am_o)
+    # GPU: one call
+    Q, D, qm, dm = h.gpu_inputs()
+    dev = "cuda"
+    scores = torch.empty(rows, cols, device=dev)
+    am = torch.empty(rows, cols, lq, dtype=torch.int32, device=dev)
+    loss = torch.empty(1, device=dev)
+    rl = torch.empty(rows, device=dev)
+    gs = torch.empty(rows, cols, device=dev)
+    gdt = Q.dtype if grads == "input" else torch.float32
+    gQ = torch.empty(Q.shape, dtype=gdt, device=dev)
+    gD = torch.empty(D.shape, dtype=gdt, device=dev)
+    tt = torch.as_tensor(target, device=dev)
+    getattr(binding, f"lik_maxsim_{layout}_ce_step")(Q, D, qm, dm, tt, scores, am, loss, rl, gs, gQ, gD, scale=scale)
+    binding.lik_check_device_error()
+    parity.assert_scores_close(scores.cpu().numpy(), s_o.reshape(rows, cols), "bf16")
+    assert abs(loss.item() - loss_o) <= parity.TOL["bf16"] * max(abs(loss_o), 1.0)
+    assert parity.normwise_rel_err(gs.cpu().numpy(), gs_o) <= parity.TOL["bf16"]
+    if np.array_equal(am.cpu().numpy().reshape(am_o.shape), am_o):
+        extra = 2.0 ** -8 if grads == "input" else 0.0
+        # the GPU's score gradient carries the bf16 bar; the backward is linear in it
+        tol = 2 * parity.TOL["bf16"] + extra
+        assert parity.normwise_rel_err(gQ.float().cpu().numpy(), gQ_o) <= tol
+        assert parity.normwise_rel_err(gD.float().cpu().numpy(), gD_o) <= tol
