@@ -176,7 +176,8 @@ class ClockSampler:
 class Step:
     """Device buffers and the liblik calls of one step of a workload."""
 
-    def __init__(self, name: str, device: torch.device, grad_dtype: str = "f32", ce: bool = False):
+    def __init__(self, name: str, device: torch.device, grad_dtype: str = "f32", ce: bool = False,
+                 recompute: bool = False):
         from late_interaction_retrieval_gb300 import binding
         self.binding = binding
         self.w = W.WORKLOADS[name]
@@ -187,6 +188,11 @@ class Step:
         self.scores = torch.empty(w.score_shape, dtype=torch.float32, device=device)
         self.argmax = (torch.empty((*w.score_shape, w.lq), dtype=torch.int32, device=device)
                        if w.backward else None)
+        # recompute: the forward saves no argmax; the backward re-runs the forward
+        # into self.argmax (its workspace) through lik_maxsim_*_bwd_recompute
+        self.recompute = recompute and w.backward
+        if self.recompute and grad_dtype != "f32":
+            raise SystemExit("--step recompute writes fp32 gradients")
         # gradients in fp32 (the default entry points) or in the inputs' dtype
         self.same_dtype = grad_dtype == "input"
         gdt = i.Q.dtype if self.same_dtype else torch.float32
@@ -218,10 +224,16 @@ class Step:
         D = i.D if D is None else D
         qm = i.qmask if qm is None else qm
         dm = i.dmask if dm is None else dm
-        getattr(self.binding, f"lik_maxsim_{self.layout}_fwd")(Q, D, qm, dm, self.scores, self.argmax)
+        getattr(self.binding, f"lik_maxsim_{self.layout}_fwd")(Q, D, qm, dm, self.scores,
+                                                               None if self.recompute else self.argmax)
 
-    def bwd(self, Q=None, D=None, g=None):
+    def bwd(self, Q=None, D=None, g=None, qm=None, dm=None):
         i = self.inp
+        if self.recompute:
+            getattr(self.binding, f"lik_maxsim_{self.layout}_bwd_recompute")(
+                i.Q if Q is None else Q, i.D if D is None else D, i.qmask if qm is None else qm,
+                i.dmask if dm is None else dm, self.g if g is None else g, self.argmax, self.gQ, self.gD)
+            return
         if self.ce:
             self.binding.lik_ce_rows(self.scores.view(self.w.nq, -1), self.target, self.loss, self.row_loss,
                                      self.g.view(self.w.nq, -1))
@@ -230,10 +242,11 @@ class Step:
             self.argmax, self.gQ, self.gD)
 
     # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours;
-    # the cross-entropy head is two kernels: per-row terms, then their mean)
+    # the cross-entropy head is two kernels: per-row terms, then their mean; the
+    # recompute backward adds one forward)
     @property
     def launches_per_step(self) -> int:
-        return 1 + (2 if self.w.backward else 0) + (2 if self.ce else 0)
+        return 1 + (2 if self.w.backward else 0) + (2 if self.ce else 0) + (1 if self.recompute else 0)
 
     def valid_flops(self) -> int:
         i, w = self.inp, self.w
@@ -269,7 +282,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
     name = args.workload
-    st = Step(name, device, args.grad_dtype, ce=args.step == "ce")
+    st = Step(name, device, args.grad_dtype, ce=args.step == "ce", recompute=args.step == "recompute")
     w = st.w
     stream = torch.cuda.current_stream(device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
@@ -360,6 +373,8 @@ def run_ours(args):
                 "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
                 "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
                 "loss_head": "cross-entropy inside the step" if st.ce else "score gradient precomputed",
+                "argmax": ("recomputed in the backward" if st.recompute else "saved by the forward")
+                          if w.backward else None,
                 "counted_flops_per_step": counted, "valid_token_flops_per_step": st.valid_flops(),
                 "algorithmic_fwd_bytes": st.algorithmic_bytes(),
                 "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
@@ -407,7 +422,7 @@ def run_e2e(st: Step, args, stream, world):
         else:
             st.fwd(dev["Q"], dev["D"], dev["qm"], dev["dm"])
             if w.backward:
-                st.bwd(dev["Q"], dev["D"], dev["g"])
+                st.bwd(dev["Q"], dev["D"], dev["g"], dev["qm"], dev["dm"])
         for o, b in zip(outs, back):
             b.copy_(o, non_blocking=True)
 
@@ -545,8 +560,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="inbatch_b128_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--step", choices=["fwd+bwd", "ce"], default="fwd+bwd",
-                    help="ce: the workload's cross-entropy head (loss and score gradient) inside every step")
+    ap.add_argument("--step", choices=["fwd+bwd", "ce", "recompute"], default="fwd+bwd",
+                    help="ce: the workload's cross-entropy head (loss and score gradient) inside every step; "
+                         "recompute: the forward saves no argmax and the backward recomputes it")
     ap.add_argument("--grad-dtype", choices=["f32", "input"], default="f32",
                     help="gradients in fp32 (default) or in the inputs' dtype (the _bwd_same_dtype entry points)")
     args = ap.parse_args()

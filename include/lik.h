@@ -203,6 +203,39 @@ lik_status lik_maxsim_kd_bwd_same_dtype(const void* Q, const void* D, lik_dtype 
                                         const float* grad_out, const int32_t* argmax,
                                         void* grad_Q, void* grad_D, cudaStream_t stream);
 
+/* ------------------------------------------- backward that recomputes argmax --
+ * For an argmax-free training forward (call the _fwd entry point with argmax
+ * = NULL, which saves only the scores; the LIK announcement thread, post
+ * 5/N, and the colpali PR's Results describe the fused path as holding only
+ * the score output between forward and backward): the backward re-runs the
+ * forward into `argmax_workspace` and then runs the _bwd entry point on it.
+ * So the int32 argmax [pairs, Lq] exists only for the duration of this call
+ * (the caller may share one workspace between calls on one stream).
+ *   qmask, dmask            as passed to the forward (the argmax depends on them)
+ *   argmax_workspace        int32 [pairs, Lq], device, 4-byte aligned, required;
+ *                           overwritten, its contents after the call are the argmax
+ *   grad_out, grad_Q, grad_D as in the _bwd entry points (fp32 gradients)
+ * Cost: one forward (with argmax) plus one backward.  Errors as in _fwd and
+ * _bwd.
+ */
+lik_status lik_maxsim_allpairs_bwd_recompute(const void* Q, const void* D, lik_dtype dtype,
+                                             int64_t Nq, int64_t Nd, int64_t Lq, int64_t Ld,
+                                             int64_t dim, const bool* qmask, const bool* dmask,
+                                             const float* grad_out, int32_t* argmax_workspace,
+                                             float* grad_Q, float* grad_D, cudaStream_t stream);
+
+lik_status lik_maxsim_pairwise_bwd_recompute(const void* Q, const void* D, lik_dtype dtype,
+                                             int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
+                                             const bool* qmask, const bool* dmask,
+                                             const float* grad_out, int32_t* argmax_workspace,
+                                             float* grad_Q, float* grad_D, cudaStream_t stream);
+
+lik_status lik_maxsim_kd_bwd_recompute(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                       int64_t N, int64_t Lq, int64_t Ld, int64_t dim,
+                                       const bool* qmask, const bool* dmask,
+                                       const float* grad_out, int32_t* argmax_workspace,
+                                       float* grad_Q, float* grad_D, cudaStream_t stream);
+
 /* --------------------------------------------------- cross-entropy head --
  * colpali PR "Add support for late-interaction-kernels (LIK)": "What this PR
  * adds" routes the in-batch ColBERT losses (a query against the batch's

@@ -37,6 +37,9 @@ SIGNATURES = {
     "lik_maxsim_allpairs_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_pairwise_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
     "lik_maxsim_kd_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_allpairs_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 7),
+    "lik_maxsim_pairwise_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 7),
+    "lik_maxsim_kd_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 7),
     "lik_ce_rows": (_I32, [_P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "lik_maxsim_allpairs_ce_step": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 3 + [ctypes.c_float]
                                     + [_P] * 7 + [_I32, _P]),
@@ -260,6 +263,49 @@ def lik_maxsim_kd_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=Non
     _check(load().lik_maxsim_kd_bwd_same_dtype(
         _ptr(Q), _ptr(D), dt, B, N, Lq, Ld, dim, _ptr(grad_out), _ptr(argmax),
         _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+# ------------------------------------------ backward that recomputes argmax --
+
+def _recompute(kind, Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q, grad_D, stream):
+    if kind == "kd":
+        dt, dev = _embeddings(Q, D, 3, 4)
+        B, Lq, dim = Q.shape
+        N, Ld = D.shape[1], D.shape[2]
+        sizes, pairs, dshape = (B, N, Lq, Ld, dim), (B, N), (B, N, Ld)
+    else:
+        dt, dev = _embeddings(Q, D, 3, 3)
+        nq, Lq, dim = Q.shape
+        nd, Ld = D.shape[0], D.shape[1]
+        if kind == "allpairs":
+            sizes, pairs = (nq, nd, Lq, Ld, dim), (nq, nd)
+        else:
+            sizes, pairs = (nq, Lq, Ld, dim), (nq,)
+        dshape = (nd, Ld)
+    _need(qmask, "qmask", (Q.shape[0], Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", dshape, torch.bool, dev, optional=True)
+    _need(grad_out, "grad_out", pairs, torch.float32, dev)
+    _need(argmax_workspace, "argmax_workspace", (*pairs, Lq), torch.int32, dev)
+    _need(grad_Q, "grad_Q", tuple(Q.shape), torch.float32, dev, optional=True)
+    _need(grad_D, "grad_D", tuple(D.shape), torch.float32, dev, optional=True)
+    _check(getattr(load(), f"lik_maxsim_{kind}_bwd_recompute")(
+        _ptr(Q), _ptr(D), dt, *sizes, _ptr(qmask), _ptr(dmask), _ptr(grad_out), _ptr(argmax_workspace),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
+
+
+def lik_maxsim_allpairs_bwd_recompute(Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q=None, grad_D=None,
+                                      stream=None):
+    _recompute("allpairs", Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q, grad_D, stream)
+
+
+def lik_maxsim_pairwise_bwd_recompute(Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q=None, grad_D=None,
+                                      stream=None):
+    _recompute("pairwise", Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q, grad_D, stream)
+
+
+def lik_maxsim_kd_bwd_recompute(Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q=None, grad_D=None,
+                                stream=None):
+    _recompute("kd", Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q, grad_D, stream)
 
 
 # --------------------------------------------------- cross-entropy head --

@@ -188,8 +188,10 @@ Problem make_problem(int layout, lik_dtype dtype, const void* Q, const void* D,
     return P;
 }
 
+// scores may be NULL only for the backward's recompute (argmax_only): the
+// kernels then write the argmax alone.
 lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float* scores,
-                   int32_t* argmax, cudaStream_t stream) {
+                   int32_t* argmax, cudaStream_t stream, bool argmax_only = false) {
     int dev = 0;
     lik_status st = check_device(&dev);
     if (st != LIK_OK) return st;
@@ -199,8 +201,8 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
         {"D", P.D, true, d_elems},
         {"qmask", qmask, false, P.n_query * P.Lq},
         {"dmask", dmask, false, P.n_doc * P.Ld},
-        {"scores", scores, true, P.n_pairs},
-        {"argmax", argmax, false, P.n_pairs * P.Lq},
+        {"scores", scores, !argmax_only, P.n_pairs},
+        {"argmax", argmax, argmax_only, P.n_pairs * P.Lq},
     };
     if ((st = check_buffers(dev, specs, 6)) != LIK_OK) return st;
     if ((st = check_alignment(P.Q, P.D)) != LIK_OK) return st;
@@ -510,6 +512,49 @@ lik_status lik_maxsim_kd_ce_step(const void* Q, const void* D, lik_dtype dtype, 
                                             stream);
     return lik_maxsim_kd_bwd(Q, D, dtype, B, N, Lq, Ld, dim, grad_scores, argmax, static_cast<float*>(grad_Q),
                              static_cast<float*>(grad_D), stream);
+}
+
+lik_status lik_maxsim_allpairs_bwd_recompute(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
+                                             int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,
+                                             const bool* qmask, const bool* dmask, const float* grad_out,
+                                             int32_t* argmax_workspace, float* grad_Q, float* grad_D,
+                                             cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, Nq, Nd, Nd, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+    if (nothing) P.n_pairs = 0;
+    if (!nothing && (st = run_fwd(P, qmask, dmask, nullptr, argmax_workspace, stream, true)) != LIK_OK) return st;
+    return run_bwd(P, grad_out, argmax_workspace, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_pairwise_bwd_recompute(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                             int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                             const bool* dmask, const float* grad_out,
+                                             int32_t* argmax_workspace, float* grad_Q, float* grad_D,
+                                             cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kPairwise, dtype, Q, D, qmask, dmask, B, B, 1, B, Lq, Ld, dim);
+    if ((st = run_fwd(P, qmask, dmask, nullptr, argmax_workspace, stream, true)) != LIK_OK) return st;
+    return run_bwd(P, grad_out, argmax_workspace, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_kd_bwd_recompute(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                                       int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                       const bool* dmask, const float* grad_out, int32_t* argmax_workspace,
+                                       float* grad_Q, float* grad_D, cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK) return st;
+    Problem P = make_problem(kKd, dtype, Q, D, qmask, dmask, B, B * N, N, B * N, Lq, Ld, dim);
+    if (nothing) P.n_pairs = 0;
+    if (!nothing && (st = run_fwd(P, qmask, dmask, nullptr, argmax_workspace, stream, true)) != LIK_OK) return st;
+    return run_bwd(P, grad_out, argmax_workspace, grad_Q, grad_D, stream);
 }
 
 }  // extern "C"

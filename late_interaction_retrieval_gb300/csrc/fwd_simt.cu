@@ -58,7 +58,7 @@ fwd_simt_kernel(Problem P, float* __restrict__ scores, int32_t* __restrict__ arg
         any = __syncthreads_or(any);
 
         if (!any) {
-            if (tid == 0) scores[p] = kEmptyDocScore;
+            if (tid == 0 && scores) scores[p] = kEmptyDocScore;
             if (argmax)
                 for (int64_t i = tid; i < P.Lq; i += kThreads) argmax[p * P.Lq + i] = -1;
             __syncthreads();
@@ -114,7 +114,7 @@ fwd_simt_kernel(Problem P, float* __restrict__ scores, int32_t* __restrict__ arg
             float sum = 0.0f;
             for (int64_t i = 0; i < P.Lq; ++i)
                 if (!qm || qm[i]) sum += best[i];
-            scores[p] = sum;
+            if (scores) scores[p] = sum;
         }
         if (argmax)
             for (int64_t i = tid; i < P.Lq; i += kThreads)

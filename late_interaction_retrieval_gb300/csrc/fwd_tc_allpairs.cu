@@ -555,7 +555,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                             s3 += t[k4 + 3];
                         }
                         for (; k4 < Lq; ++k4) s0 += t[k4];
-                        p.scores[pair] = any_doc ? (s0 + s1) + (s2 + s3) : kEmptyDocScore;
+                        if (p.scores) p.scores[pair] = any_doc ? (s0 + s1) + (s2 + s3) : kEmptyDocScore;
                     }
                     if (p.argmax) p.argmax[pair * Lq + iq[k]] = am[k];
                 }

@@ -530,7 +530,7 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
                 if (!ok) break;
             }
             if (!ok) break;
-            if (quarter == 0 && lane == 0) p.scores[pair] = info.nonempty ? total : kEmptyDocScore;
+            if (quarter == 0 && lane == 0 && p.scores) p.scores[pair] = info.nonempty ? total : kEmptyDocScore;
             ptx::mbar_arrive(ptx::smem_u32(&bars->dump_empty[db]));
             if (++db == 2) { db = 0; dph ^= 1; }
         }
