@@ -236,6 +236,30 @@ lik_status lik_maxsim_kd_bwd_recompute(const void* Q, const void* D, lik_dtype d
                                        const float* grad_out, int32_t* argmax_workspace,
                                        float* grad_Q, float* grad_D, cudaStream_t stream);
 
+/*
+ * The same all-pairs recompute backward for callers that cannot allocate
+ * device memory (for example a memory manager that owns the whole device,
+ * or a loop that cannot pay for cudaMalloc): the argmax workspace is an
+ * array built into the library, 2^21 int32 entries (8 MiB), held on every
+ * GPU that loads the library until the process exits.  The pages have no
+ * counterpart to this entry point.
+ *   - Nq * Nd * Lq <= 2097152, else LIK_ERR_UNSUPPORTED (nothing launched).
+ *   - Nothing is allocated.  The first call on a device, with that device
+ *     current, looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - Every call shares the array; calls whose work overlaps on the GPU
+ *     race on it, so order them (one stream, or events).  Its contents need
+ *     no clearing: the forward writes every entry the backward reads.
+ *   - Other arguments, outputs and errors as in
+ *     lik_maxsim_allpairs_bwd_recompute.
+ */
+lik_status lik_maxsim_allpairs_bwd_recompute_noalloc(const void* Q, const void* D,
+                                                     lik_dtype dtype, int64_t Nq, int64_t Nd,
+                                                     int64_t Lq, int64_t Ld, int64_t dim,
+                                                     const bool* qmask, const bool* dmask,
+                                                     const float* grad_out, float* grad_Q,
+                                                     float* grad_D, cudaStream_t stream);
+
 /* --------------------------------------------------- cross-entropy head --
  * colpali PR "Add support for late-interaction-kernels (LIK)": "What this PR
  * adds" routes the in-batch ColBERT losses (a query against the batch's

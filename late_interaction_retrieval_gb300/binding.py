@@ -40,6 +40,7 @@ SIGNATURES = {
     "lik_maxsim_allpairs_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 7),
     "lik_maxsim_pairwise_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 7),
     "lik_maxsim_kd_bwd_recompute": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 7),
+    "lik_maxsim_allpairs_bwd_recompute_noalloc": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 6),
     "lik_ce_rows": (_I32, [_P, _I64, _I64, _P, ctypes.c_float, _P, _P, _P, _P]),
     "lik_maxsim_allpairs_ce_step": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 3 + [ctypes.c_float]
                                     + [_P] * 7 + [_I32, _P]),
@@ -306,6 +307,23 @@ def lik_maxsim_pairwise_bwd_recompute(Q, D, qmask, dmask, grad_out, argmax_works
 def lik_maxsim_kd_bwd_recompute(Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q=None, grad_D=None,
                                 stream=None):
     _recompute("kd", Q, D, qmask, dmask, grad_out, argmax_workspace, grad_Q, grad_D, stream)
+
+
+def lik_maxsim_allpairs_bwd_recompute_noalloc(Q, D, qmask, dmask, grad_out, grad_Q=None, grad_D=None,
+                                              stream=None):
+    """The all-pairs recompute backward with the library's built-in argmax
+    workspace (no device memory is allocated; Nq * Nd * Lq <= 2**21)."""
+    dt, dev = _embeddings(Q, D, 3, 3)
+    nq, Lq, dim = Q.shape
+    nd, Ld = D.shape[0], D.shape[1]
+    _need(qmask, "qmask", (nq, Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", (nd, Ld), torch.bool, dev, optional=True)
+    _need(grad_out, "grad_out", (nq, nd), torch.float32, dev)
+    _need(grad_Q, "grad_Q", tuple(Q.shape), torch.float32, dev, optional=True)
+    _need(grad_D, "grad_D", tuple(D.shape), torch.float32, dev, optional=True)
+    _check(load().lik_maxsim_allpairs_bwd_recompute_noalloc(
+        _ptr(Q), _ptr(D), dt, nq, nd, Lq, Ld, dim, _ptr(qmask), _ptr(dmask), _ptr(grad_out),
+        _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
 
 
 # --------------------------------------------------- cross-entropy head --

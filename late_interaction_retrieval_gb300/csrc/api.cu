@@ -56,6 +56,10 @@ lik_status cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+// For entry points defined in other files: records `message` as the calling
+// thread's lik_last_error_message() and returns `s`.
+lik_status report_status(lik_status s, const char* message) { return fail(s, "%s", message); }
+
 const DeviceInfo& device_info(int device) {
     DeviceSlot& slot = g_devices[device % kMaxDevices];
     std::call_once(slot.once, [&] {
