@@ -242,11 +242,13 @@ class Step:
             self.argmax, self.gQ, self.gD)
 
     # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours;
-    # the cross-entropy head is two kernels: per-row terms, then their mean; the
-    # recompute backward adds one forward)
+    # the streaming forward of the pairwise and kd layouts is a plan kernel and
+    # the forward kernel; the cross-entropy head is two kernels: per-row terms,
+    # then their mean; the recompute backward adds one forward)
     @property
     def launches_per_step(self) -> int:
-        return 1 + (2 if self.w.backward else 0) + (2 if self.ce else 0) + (1 if self.recompute else 0)
+        fwd = 1 if self.layout == "allpairs" else 2
+        return fwd + (2 if self.w.backward else 0) + (2 if self.ce else 0) + (fwd if self.recompute else 0)
 
     def valid_flops(self) -> int:
         i, w = self.inp, self.w

@@ -40,8 +40,14 @@
  *     the current device, row-major and contiguous.  Q, D, grad_Q and grad_D
  *     must be 16-byte aligned; scores, argmax and grad_out 4-byte aligned.
  *     Host pointers are rejected with LIK_ERR_INVALID_ARG.
- *   - The caller allocates every buffer, outputs included.  The library
- *     allocates no device memory and keeps no per-call state.
+ *   - The caller allocates every buffer, outputs included.  The one device
+ *     allocation the library makes is the workspace of the fp16/bf16 pairwise
+ *     and kd forward (the streaming kernel's schedule: with a document mask,
+ *     4 bytes per pair and 16 bytes per 128-token document tile; always
+ *     about 0.5 KB per SM), taken with cudaMallocFromPoolAsync from a
+ *     library-owned memory pool of the device and released with cudaFreeAsync
+ *     on `stream` after the kernel.  The pool keeps the memory it has mapped
+ *     for later calls.  The library keeps no other per-call state.
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *     Outputs are complete when the stream reaches the call.  Gradients are
  *     overwritten, not accumulated into.
@@ -142,6 +148,9 @@ lik_status lik_maxsim_allpairs_bwd(const void* Q, const void* D, lik_dtype dtype
  * product").
  *   Q [B, Lq, dim], D [B, Ld, dim], qmask [B, Lq], dmask [B, Ld],
  *   scores [B], argmax [B, Lq] (or NULL)
+ * fp16/bf16 with dim % 16 == 0, dim <= 256 and Lq <= 32 take the streaming
+ * tensor-core kernel: a plan kernel over the document mask, then the forward,
+ * both on `stream`, with the pooled workspace described above.
  */
 lik_status lik_maxsim_pairwise_fwd(const void* Q, const void* D, lik_dtype dtype,
                                    int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
@@ -160,6 +169,7 @@ lik_status lik_maxsim_pairwise_bwd(const void* Q, const void* D, lik_dtype dtype
  * negative-document losses): query b against its own N candidates.
  *   Q [B, Lq, dim], D [B, N, Ld, dim], qmask [B, Lq], dmask [B, N, Ld],
  *   scores [B, N], argmax [B, N, Lq] (or NULL)
+ * The same streaming kernel (and workspace) as the pairwise layout.
  */
 lik_status lik_maxsim_kd_fwd(const void* Q, const void* D, lik_dtype dtype,
                              int64_t B, int64_t N, int64_t Lq, int64_t Ld, int64_t dim,

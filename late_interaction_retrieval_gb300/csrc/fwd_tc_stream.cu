@@ -186,27 +186,26 @@ __device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
 }
 
 // Index of the last nonzero byte of row[0, n), or -1 (one warp, every lane
-// gets the result).  Scans backwards: the bytes after the last 16-byte
-// boundary, then 16-byte words 128 at a time (four loads in flight per lane),
-// then the bytes before the first boundary.  Every access lies in row[0, n).
+// gets the result).  The bytes after the last 16-byte boundary, the last 128
+// 16-byte words (four per lane) and the bytes before the first boundary are
+// loaded together, then looked at from the end; further words (rows longer
+// than 2 KB with a long invalid tail) 128 at a time.  Every access lies in
+// row[0, n).
 __device__ int64_t last_nonzero_byte(const uint8_t* row, int64_t n, int lane) {
     int64_t head = static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15);
     if (head > n) head = n;
     const int64_t words = (n - head) / 16;
     const int64_t tail0 = head + 16 * words;
-    int64_t best = -1;
-    if (tail0 + lane < n && row[tail0 + lane] != 0) best = tail0 + lane;
-    best = warp_max_i64(best);
-    if (best >= 0) return best;
     const uint4* wv = reinterpret_cast<const uint4*>(row + head);
-    for (int64_t top = words; top > 0; top -= 128) {
-        uint4 v[4];
-        int64_t wi[4];
+    auto load_words = [&](int64_t top, uint4 (&v)[4], int64_t (&wi)[4]) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             wi[k] = top - 1 - lane - 32 * k;
             v[k] = wi[k] >= 0 ? wv[wi[k]] : make_uint4(0, 0, 0, 0);
         }
+    };
+    auto last_in_words = [&](const uint4 (&v)[4], const int64_t (&wi)[4]) {
+        int64_t best = -1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t x[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
@@ -220,11 +219,21 @@ __device__ int64_t last_nonzero_byte(const uint8_t* row, int64_t n, int lane) {
                 }
             }
         }
-        best = warp_max_i64(best);
+        return warp_max_i64(best);
+    };
+    const uint8_t tb = tail0 + lane < n ? row[tail0 + lane] : uint8_t(0);
+    const uint8_t hb = lane < head ? row[lane] : uint8_t(0);
+    uint4 v[4];
+    int64_t wi[4];
+    load_words(words, v, wi);
+    int64_t best = warp_max_i64(tb != 0 ? tail0 + lane : -1);
+    if (best >= 0) return best;
+    for (int64_t top = words; top > 0; top -= 128) {
+        if (top != words) load_words(top, v, wi);
+        best = last_in_words(v, wi);
         if (best >= 0) return best;
     }
-    if (lane < head && row[lane] != 0) best = lane;
-    return warp_max_i64(best);
+    return warp_max_i64(hb != 0 ? static_cast<int64_t>(lane) : -1);
 }
 
 // Plan kernel, two kinds of blocks of 1024 threads (with a document mask):

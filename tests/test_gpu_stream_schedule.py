@@ -113,3 +113,21 @@ def test_cut_documents_on_two_streams_at_once():
     for (s_a, am_a), (s, am, *_rest) in zip(alone, bufs):
         assert np.array_equal(s.cpu().numpy(), s_a)
         assert np.array_equal(am.cpu().numpy(), am_a)
+
+
+@pytest.mark.parametrize("layout,nq,nd,ld", [("pairwise", 10, 10, 1030), ("pairwise", 6, 6, 5000),
+                                             ("kd", 2, 5, 1031)])
+def test_scattered_document_masks(layout, nq, nd, ld):
+    """Masks that are not prefixes: Bernoulli tokens, a document valid only at
+    its first token, only at its last, at one token in the middle, and empty
+    (rows of odd length start at every alignment, so the plan's scan meets
+    every head and tail case)."""
+    inp = random_case(layout, nq, nd, 32, ld, 128, "bf16", seed=ld + 7)
+    g = torch.Generator().manual_seed(ld)
+    dm = (torch.rand(inp.dmask.shape, generator=g) < 0.3)
+    flat = dm.view(-1, ld)
+    special = [lambda r: r.zero_().__setitem__(0, True), lambda r: r.zero_().__setitem__(ld - 1, True),
+               lambda r: r.zero_().__setitem__(ld // 2, True), lambda r: r.zero_()]
+    for k, f in enumerate(special):
+        f(flat[k])
+    gpu_harness.Layout(dataclasses.replace(inp, dmask=dm)).check_forward()
