@@ -18,9 +18,10 @@
 // Tiling.  A tile is 128 consecutive tokens of one document (TMA box of a
 // 3D map [n_doc, Ld, dim]; tokens past Ld read as zero).  The MMA puts the
 // document tokens on the M side and the query's tokens on the N side:
-//     S[128, Np] = Dtile[128, dim] . Qb[Np, dim]^T    (fp32 in TMEM)
-// with Np = Lq rounded up to 16.  So each accumulator lane is one document
-// token and each column one query token.
+//     S[128, 32] = Dtile[128, dim] . Qb[32, dim]^T    (fp32 in TMEM)
+// with the query's Lq <= 32 tokens in the first Lq columns (the rest are
+// ignored).  So each accumulator lane is one document token and each column
+// one query token.
 //
 // Schedule.  A document's work is its tiles up to the last one holding a
 // valid token (at least one, so an empty document still gets its -1e9); a
@@ -35,15 +36,14 @@
 //
 // Roles (one CTA per SM, persistent over its range of tiles; 224 threads):
 //   warp 0      producer.  Finds the CTA's range (a search over the plan's
-//               per-group sums), then all 32 lanes read the document mask a
-//               window of 8 tiles ahead and build each tile's 128-bit
-//               row-validity mask (one ballot per 32 rows); tiles with no
-//               valid token are skipped (never loaded).  Lane 0 issues the
-//               TMA loads (a query's rows into one of two buffers when the
-//               query changes, document tiles per stage) and publishes,
-//               through a ring of tile records, the sequence the epilogue
-//               follows: data tiles, one end record per document piece, and
-//               an end-of-stream record.
+//               per-group sums).  Each lane loads the plan's row-validity
+//               words of one tile of the window 8 tiles ahead; tiles with no
+//               valid token are skipped (never loaded).  Lane 0 alone then
+//               issues the window's TMA loads (a query's rows into one of two
+//               buffers when the query changes, document tiles per stage) and
+//               publishes, through a ring of tile records, the sequence the
+//               epilogue follows: data tiles, one end record per document
+//               piece, and an end-of-stream record.
 //   warp 1      TMEM allocator + single-thread MMA issuer (4 accumulators).
 //   warps 2-5   update warps.  Each thread owns one accumulator lane
 //               (document token) and keeps a running (max, argmax) for each
