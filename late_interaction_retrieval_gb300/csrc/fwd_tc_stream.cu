@@ -176,64 +176,55 @@ __device__ __forceinline__ int64_t query_of(const Params& p, int64_t pair) {
     return pair / p.pairs_per_query;
 }
 
-__device__ __forceinline__ int64_t warp_max_i64(int64_t v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const int64_t t = __shfl_xor_sync(0xffffffffu, v, off);
-        v = t > v ? t : v;
-    }
-    return v;
-}
-
 // Index of the last nonzero byte of row[0, n), or -1 (one warp, every lane
 // gets the result).  The bytes after the last 16-byte boundary, the last 128
 // 16-byte words (four per lane) and the bytes before the first boundary are
 // loaded together, then looked at from the end; further words (rows longer
 // than 2 KB with a long invalid tail) 128 at a time.  Every access lies in
-// row[0, n).
-__device__ int64_t last_nonzero_byte(const uint8_t* row, int64_t n, int lane) {
-    int64_t head = static_cast<int64_t>((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15);
+// row[0, n); n < 2^31 (the streaming kernels' limit on Ld), so offsets are
+// 32-bit.
+__device__ int last_nonzero_byte(const uint8_t* row, int n, int lane) {
+    int head = static_cast<int>((16 - (reinterpret_cast<uintptr_t>(row) & 15)) & 15);
     if (head > n) head = n;
-    const int64_t words = (n - head) / 16;
-    const int64_t tail0 = head + 16 * words;
+    const int words = (n - head) / 16;
+    const int tail0 = head + 16 * words;
     const uint4* wv = reinterpret_cast<const uint4*>(row + head);
-    auto load_words = [&](int64_t top, uint4 (&v)[4], int64_t (&wi)[4]) {
+    auto load_words = [&](int top, uint4 (&v)[4], int (&wi)[4]) {
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             wi[k] = top - 1 - lane - 32 * k;
             v[k] = wi[k] >= 0 ? wv[wi[k]] : make_uint4(0, 0, 0, 0);
         }
     };
-    auto last_in_words = [&](const uint4 (&v)[4], const int64_t (&wi)[4]) {
-        int64_t best = -1;
+    auto last_in_words = [&](const uint4 (&v)[4], const int (&wi)[4]) {
+        int best = -1;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const uint32_t x[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
             for (int e = 3; e >= 0; --e) {
                 if (x[e] != 0) {
-                    const int64_t byte = 4 * e + ((31 - __clz(static_cast<int>(x[e]))) >> 3);
-                    const int64_t at = head + 16 * wi[k] + byte;
+                    const int at = head + 16 * wi[k] + 4 * e + ((31 - __clz(static_cast<int>(x[e]))) >> 3);
                     best = at > best ? at : best;
                     break;
                 }
             }
         }
-        return warp_max_i64(best);
+        return __reduce_max_sync(0xffffffffu, best);
     };
     const uint8_t tb = tail0 + lane < n ? row[tail0 + lane] : uint8_t(0);
     const uint8_t hb = lane < head ? row[lane] : uint8_t(0);
     uint4 v[4];
-    int64_t wi[4];
+    int wi[4];
     load_words(words, v, wi);
-    int64_t best = warp_max_i64(tb != 0 ? tail0 + lane : -1);
+    int best = __reduce_max_sync(0xffffffffu, tb != 0 ? tail0 + lane : -1);
     if (best >= 0) return best;
-    for (int64_t top = words; top > 0; top -= 128) {
+    for (int top = words; top > 0; top -= 128) {
         if (top != words) load_words(top, v, wi);
         best = last_in_words(v, wi);
         if (best >= 0) return best;
     }
-    return warp_max_i64(hb != 0 ? static_cast<int64_t>(lane) : -1);
+    return __reduce_max_sync(0xffffffffu, hb != 0 ? lane : -1);
 }
 
 // Plan kernel, two kinds of blocks of 1024 threads (with a document mask):
@@ -267,7 +258,7 @@ __global__ void __launch_bounds__(1024) stream_plan_kernel(const PlanArgs a) {
         const int64_t pair = static_cast<int64_t>(blockIdx.x) * 32 + warp;
         int32_t u = 0;
         if (pair < a.n_pairs) {
-            const int64_t last = last_nonzero_byte(a.dmask + pair * a.Ld, a.Ld, lane);
+            const int last = last_nonzero_byte(a.dmask + pair * a.Ld, static_cast<int>(a.Ld), lane);
             u = last < 0 ? 1 : static_cast<int32_t>(last / kRows) + 1;
             if (lane == 0) a.units[pair] = u;
         }
@@ -284,19 +275,23 @@ __global__ void __launch_bounds__(1024) stream_plan_kernel(const PlanArgs a) {
     const int64_t total = a.n_pairs * a.tiles;
     const int64_t t0 = ((static_cast<int64_t>(blockIdx.x) - a.n_groups) * 32 + warp) * 8;
     if (t0 >= total) return;
-    int64_t pair = t0 / a.tiles, tt = t0 - pair * a.tiles;
+    // one row pointer per document and 32-bit offsets within it (Ld < 2^31)
+    const int64_t pair = t0 / a.tiles;
+    int tt = static_cast<int>(t0 - pair * a.tiles);
+    const int ld = static_cast<int>(a.Ld), tiles = static_cast<int>(a.tiles);
+    const int n_in = total - t0 < 8 ? static_cast<int>(total - t0) : 8;
+    const uint8_t* row = a.dmask + pair * a.Ld;
     uint8_t b[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const bool in = t0 + i < total;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int64_t j = tt * kRows + 32 * k + lane;
-            b[i][k] = in && j < a.Ld ? a.dmask[pair * a.Ld + j] : uint8_t(0);
+            const int j = tt * kRows + 32 * k + lane;
+            b[i][k] = i < n_in && j < ld ? row[j] : uint8_t(0);
         }
-        if (++tt == a.tiles) {
+        if (++tt == tiles) {
             tt = 0;
-            ++pair;
+            row += a.Ld;
         }
     }
 #pragma unroll
@@ -304,7 +299,7 @@ __global__ void __launch_bounds__(1024) stream_plan_kernel(const PlanArgs a) {
         uint32_t w[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) w[k] = __ballot_sync(0xffffffffu, b[i][k] != 0);
-        if (lane == i && t0 + i < total) a.words[t0 + i] = make_uint4(w[0], w[1], w[2], w[3]);
+        if (lane == i && i < n_in) a.words[t0 + i] = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
