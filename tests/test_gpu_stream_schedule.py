@@ -131,3 +131,20 @@ def test_scattered_document_masks(layout, nq, nd, ld):
     for k, f in enumerate(special):
         f(flat[k])
     gpu_harness.Layout(dataclasses.replace(inp, dmask=dm)).check_forward()
+
+
+def test_more_than_256_groups_of_pairs():
+    """Over 8192 pairs: the range search reads the per-group unit sums in
+    several passes."""
+    inp = random_case("kd", 300, 31, 16, 40, 64, "bf16", seed=31, p_doc_empty=0.1)
+    assert inp.D.shape[0] * inp.D.shape[1] > 32 * 256
+    gpu_harness.Layout(inp).check_forward()
+
+
+def test_fewer_units_than_ctas():
+    """Long padded rows with short documents: every pair has one unit, so
+    there are fewer units than CTAs and some CTAs get nothing."""
+    inp = random_case("pairwise", 100, 100, 32, 1000, 128, "bf16", seed=41, p_doc_empty=0.1)
+    dm = inp.dmask.clone()
+    dm[:, 64:] = False
+    gpu_harness.Layout(dataclasses.replace(inp, dmask=dm)).check_forward()
