@@ -255,6 +255,51 @@ def random_case(layout: str, nq: int, nd: int, lq: int, ld: int, dim: int, dtype
     return Inputs(w, Q, D, qmask, dmask, grad_out, None)
 
 
+def separated_case(layout: str, nq: int, nd: int, lq: int, ld: int, dim: int, dtype: str,
+                   seed: int, device="cpu", p_doc_empty=0.0, p_query_tail=0.5,
+                   background=0.25) -> Inputs:
+    """A random case in which every query token has one clear best document token.
+
+    Drawn as :func:`random_case` (every non-empty document long enough to hold
+    the copies below), then, with a second generator seeded from ``seed``:
+    every document token is scaled by ``background``, and for every pair
+    (q, d) of the layout each token Q[q, i] gets a copy Q[q, i] * s,
+    s ~ U[0.6, 1.0], at its own random valid position of document d.  The
+    copy's similarity is s * |Q[q, i]|^2 >= 0.6 (tokens are unit-norm), while
+    every other valid token of d is a background token or a scaled copy of
+    another token, whose similarity is a cosine of two independent random
+    directions (standard deviation 1/sqrt(dim)).  With dim >= 64 the best and
+    second-best similarities are then far apart (> 1e-2) for every valid
+    query token, which a test must still check on its own inputs; the argmax
+    of such inputs is unique and the same in any accumulation order.
+    """
+    per_doc = nq if layout == "allpairs" else 1
+    if lq * per_doc > ld:
+        raise ValueError("documents are too short for one copy per query token")
+    inp = random_case(layout, nq, nd, lq, ld, dim, dtype, seed, device, p_doc_empty, p_query_tail,
+                      min_dlen=lq * per_doc)
+    gen = generator(seed + 7919, device)
+    n_docs = math.prod(inp.workload.d_shape[:-2])
+    D = inp.D.reshape(n_docs, ld, dim).to(torch.float32) * background
+    dlen = inp.dmask.reshape(n_docs, ld).sum(dim=1)
+    Qf = inp.Q.to(torch.float32)
+    for doc in range(n_docs):
+        L = int(dlen[doc])
+        if L == 0:
+            continue
+        if layout == "allpairs":
+            src = Qf.reshape(nq * lq, dim)
+        elif layout == "kd":
+            src = Qf[doc // nd]
+        else:
+            src = Qf[doc]
+        pos = torch.randperm(L, generator=gen, device=device)[:src.shape[0]]
+        s = 0.6 + 0.4 * torch.rand(src.shape[0], generator=gen, device=device)
+        D[doc, pos] = src * s[:, None]
+    inp.D = D.to(inp.D.dtype).reshape(inp.workload.d_shape).contiguous()
+    return inp
+
+
 def to_numpy(t: torch.Tensor):
     """(array, dtype tag) in the form the oracle accepts; bf16 as uint16 bits."""
     t = t.detach().cpu().contiguous()

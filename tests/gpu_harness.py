@@ -3,7 +3,11 @@ fp64 oracle, and compare them with the rules in ``parity.py``.
 
 Inputs always come from the seeded generators; the oracle never receives a
 value the CUDA library produced.  The backward is checked on the oracle's own
-argmax, fed to both sides.
+argmax, fed to both sides.  Where the GPU computes its own argmax inside a
+call (autograd layers, recompute, loss-head steps), the inputs come from
+``separated_case``: their argmax is unique, the GPU's must equal the
+oracle's exactly, and the gradients are compared with the oracle's on every
+run, with no condition.
 """
 from __future__ import annotations
 
@@ -50,6 +54,18 @@ class Layout:
         Dn, _ = to_numpy(self.inp.D)
         qm, dm = _np_mask(self.inp.qmask), _np_mask(self.inp.dmask)
         return getattr(oracle.get(), f"{self.kind}_fwd")(Qn, Dn, qm, dm, dtype=tag)
+
+    def oracle_fwd_separated(self):
+        """The oracle forward of inputs drawn by ``separated_case``, after
+        checking what such inputs promise: every valid query token of a
+        non-empty document has a best similarity more than GAP_EXACT above
+        its second best.  The argmax is then unique, so the GPU must return
+        exactly the oracle's and both backwards run on the same indices."""
+        s, am, gap = self.oracle_fwd()
+        live = am >= 0
+        assert live.any(), "separated inputs with no live query token"
+        assert float(gap[live].min()) > parity.GAP_EXACT, "inputs are not separated"
+        return s, am, gap
 
     def oracle_bwd(self, grad_out, argmax):
         Qn, tag = to_numpy(self.inp.Q)

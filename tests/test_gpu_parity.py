@@ -15,7 +15,7 @@ import torch
 import gpu_harness
 import parity
 from late_interaction_retrieval_gb300 import binding, layers
-from late_interaction_retrieval_gb300.workloads import Inputs, Workload, generate, random_case
+from late_interaction_retrieval_gb300.workloads import Inputs, Workload, generate, random_case, separated_case
 
 pytestmark = pytest.mark.gpu
 
@@ -165,28 +165,34 @@ def test_zero_padding_differs_from_mask():
 
 # -------------------------------------------------------- autograd path --
 
-@pytest.mark.parametrize("dtype", ["bf16", "f32"])
-def test_autograd_layers(dtype):
-    inp = random_case("allpairs", 4, 6, 32, 150, 128, dtype, seed=21, p_doc_empty=0.2)
+@pytest.mark.parametrize("layout", ["allpairs", "pairwise", "kd"])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_autograd_layers(layout, dtype):
+    """Forward and backward through the autograd layers against the oracle,
+    on inputs whose argmax is unique (the GPU's own argmax must then be the
+    oracle's), with the gradients compared on every run."""
+    ld = 150 if layout != "allpairs" else 160
+    inp = separated_case(layout, 4, 5, 32, ld, 128, dtype, seed=21, p_doc_empty=0.2)
     h = gpu_harness.Layout(inp)
-    s_o, am_o, _ = h.oracle_fwd()
+    s_o, am_o, _ = h.oracle_fwd_separated()
     Q, D, qm, dm = h.gpu_inputs()
     Q.requires_grad_(True)
     D.requires_grad_(True)
-    scores = layers.MaxSim()(Q, D, qm, dm)
+    layer = {"allpairs": layers.MaxSim, "pairwise": layers.MaxSimPairwise, "kd": layers.MaxSimKD}[layout]
+    scores = layer()(Q, D, qm, dm)
     g = inp.grad_out.cuda()
     scores.backward(g)
     parity.assert_scores_close(scores.detach().cpu().numpy(), s_o, dtype)
-    # compare gradients only when the GPU picked the oracle's argmax everywhere
     _, am_g = h.gpu_fwd()
-    if np.array_equal(am_g, am_o):
-        gQ_o, gD_o = h.oracle_bwd(inp.grad_out.numpy().astype(np.float64), am_o)
-        # the layer hands autograd gradients in the input dtype: one extra
-        # rounding to bf16 costs up to 2^-8 relative on top of the kernel's bar
-        extra = 2.0 ** -8 if dtype == "bf16" else 0.0
-        for got, ref, name in ((Q.grad, gQ_o, "grad_Q"), (D.grad, gD_o, "grad_D")):
-            err = parity.normwise_rel_err(got.float().cpu().numpy(), ref)
-            assert err <= parity.TOL[dtype] + extra, (name, err)
+    assert np.array_equal(am_g.reshape(am_o.shape), am_o), "argmax differs on separated inputs"
+    gQ_o, gD_o = h.oracle_bwd(inp.grad_out.numpy().astype(np.float64), am_o)
+    # the layer hands autograd gradients in the input dtype: one extra
+    # rounding to 16 bits costs up to 2^-8 (bf16) / 2^-11 (fp16) relative on
+    # top of the kernel's bar
+    extra = {"bf16": 2.0 ** -8, "f16": 2.0 ** -11, "f32": 0.0}[dtype]
+    for got, ref, name in ((Q.grad, gQ_o, "grad_Q"), (D.grad, gD_o, "grad_D")):
+        err = parity.normwise_rel_err(got.float().cpu().numpy(), ref)
+        assert err <= parity.TOL[dtype] + extra, (name, err)
     assert Q.grad.dtype == Q.dtype and D.grad.dtype == D.dtype
 
 
