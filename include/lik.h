@@ -44,14 +44,24 @@
  *     allocation the library makes is the workspace of the fp16/bf16 pairwise
  *     and kd forward (the streaming kernel's schedule: with a document mask,
  *     4 bytes per pair and 16 bytes per 128-token document tile; always
- *     about 0.5 KB per SM), taken with cudaMallocFromPoolAsync from a
- *     library-owned memory pool of the device and released with cudaFreeAsync
- *     on `stream` after the kernel.  The pool keeps the memory it has mapped
- *     for later calls.  The library keeps no other per-call state.
+ *     about 0.5 KB per SM) when the caller does not pass one: the
+ *     lik_maxsim_{pairwise,kd}_fwd_ws entry points take it from the caller
+ *     (its size from lik_maxsim_{pairwise,kd}_fwd_workspace_bytes) and
+ *     allocate nothing; the plain _fwd entry points take it with
+ *     cudaMallocFromPoolAsync from a library-owned memory pool of the device
+ *     and release it with cudaFreeAsync on `stream` after the kernel.  The
+ *     pool keeps the memory it has mapped for later calls.  The library keeps
+ *     no other per-call state.
  *   - Calls are asynchronous on `stream` (0 = the legacy default stream).
  *     Outputs are complete when the stream reaches the call.  Gradients are
  *     overwritten, not accumulated into.
  *   - Functions are thread-safe.
+ *   - Per device, the library looks up the device addresses of its own
+ *     status word (and of the no-allocation entry point's array, below) on
+ *     its first call with that device current and keeps them for the
+ *     process's life.  Resetting the device (cudaDeviceReset) after that
+ *     invalidates them: a process that resets a device must not call the
+ *     library on it again.
  *
  * Errors:
  *   - LIK_ERR_INVALID_ARG: a negative size, a NULL required pointer, a host
@@ -75,6 +85,7 @@
 #define LIK_H
 
 #include <stdbool.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include <cuda_runtime_api.h>
@@ -115,9 +126,25 @@ const char* lik_version(void);
  */
 lik_status lik_check_device_error(cudaStream_t stream);
 
+/*
+ * Self-test of the failure path of the kernels' bounded waits.  Launches on
+ * `stream` one thread that waits, with the same bounded mbarrier wait the
+ * tensor-core pipelines use and a limit of `timeout_us` microseconds, on an
+ * mbarrier that nothing ever arrives at; when the limit passes it sets the
+ * device error word and returns.  A following lik_check_device_error(stream)
+ * must then return LIK_ERR_TIMEOUT (and clear the word), and the context
+ * stays usable.  No copy, MMA or tensor memory is involved.  The pages have
+ * no counterpart to this entry point; it exists to test that a wait that
+ * runs out reaches the caller as a status (colpali PR "Add support for
+ * late-interaction-kernels (LIK)", Design section: kernel failures are
+ * reported, never hidden).
+ *   timeout_us  1 .. 1000000, else LIK_ERR_INVALID_ARG (nothing launched)
+ */
+lik_status lik_selftest_bounded_wait(int64_t timeout_us, cudaStream_t stream);
+
 /* ------------------------------------------------------------ all-pairs --
  * README "Scoring interface" table, layer MaxSim: every query against every
- * document ("for example for in-batch training").
+ * document, the layout of in-batch contrastive training.
  *   Q      [Nq, Lq, dim]   dtype
  *   D      [Nd, Ld, dim]   dtype
  *   qmask  [Nq, Lq]        or NULL
@@ -144,8 +171,8 @@ lik_status lik_maxsim_allpairs_bwd(const void* Q, const void* D, lik_dtype dtype
 
 /* ------------------------------------------------------------- pairwise --
  * README "Scoring interface" table, layer MaxSimPairwise: query b against
- * document b only ("for reranking, without computing the full cross
- * product").
+ * document b only, the reranking layout, with no query-by-document cross
+ * product computed.
  *   Q [B, Lq, dim], D [B, Ld, dim], qmask [B, Lq], dmask [B, Ld],
  *   scores [B], argmax [B, Lq] (or NULL)
  * fp16/bf16 with dim % 16 == 0, dim <= 256 and Lq <= 32 take the streaming
@@ -163,6 +190,38 @@ lik_status lik_maxsim_pairwise_bwd(const void* Q, const void* D, lik_dtype dtype
                                    const float* grad_out, const int32_t* argmax,
                                    float* grad_Q, float* grad_D, cudaStream_t stream);
 
+/* ------------------------------------- caller-provided forward workspace --
+ * The pairwise and kd forward with its schedule workspace supplied by the
+ * caller, so that the library allocates no device memory at all: for a
+ * caller that manages every byte of device memory itself.  The pages have
+ * no counterpart; their layers (README, "Scoring interface") take only the
+ * operator's own tensors.
+ *
+ * lik_maxsim_{pairwise,kd}_fwd_workspace_bytes writes to *bytes the size of
+ * the workspace the matching _fwd_ws call needs for these sizes, dtype and
+ * whether a document mask is passed (has_dmask != 0), on the current device
+ * (it depends on the device's SM count); 0 when the call takes a kernel
+ * that needs none (fp32 inputs, shapes outside the streaming kernel's
+ * limits).  It launches nothing.
+ *
+ * lik_maxsim_{pairwise,kd}_fwd_ws: the _fwd entry point with
+ *   workspace        device memory of the current device, 16-byte aligned,
+ *                    at least the queried size (may be NULL when that is 0);
+ *                    overwritten; no contents need to survive between calls
+ *   workspace_bytes  its size
+ * A workspace that is NULL, too small, misaligned or not device memory gives
+ * LIK_ERR_INVALID_ARG and nothing is launched.  Calls that overlap on the
+ * GPU must not share a workspace (order them, or give each its own).  The
+ * results are bit-identical to the _fwd entry point's.
+ */
+lik_status lik_maxsim_pairwise_fwd_workspace_bytes(lik_dtype dtype, int64_t B, int64_t Lq, int64_t Ld,
+                                                  int64_t dim, int has_dmask, size_t* bytes);
+
+lik_status lik_maxsim_pairwise_fwd_ws(const void* Q, const void* D, lik_dtype dtype, int64_t B,
+                                      int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                      const bool* dmask, float* scores, int32_t* argmax,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------- per-query candidates --
  * colpali PR "Add support for late-interaction-kernels (LIK)", Design
  * section (maxsim_kd, the per-query candidate layout used by the
@@ -176,6 +235,16 @@ lik_status lik_maxsim_kd_fwd(const void* Q, const void* D, lik_dtype dtype,
                              const bool* qmask, const bool* dmask,
                              float* scores, int32_t* argmax, cudaStream_t stream);
 
+/* The kd forward with a caller-provided workspace: see the pairwise
+ * _fwd_workspace_bytes / _fwd_ws entry points above. */
+lik_status lik_maxsim_kd_fwd_workspace_bytes(lik_dtype dtype, int64_t B, int64_t N, int64_t Lq,
+                                            int64_t Ld, int64_t dim, int has_dmask, size_t* bytes);
+
+lik_status lik_maxsim_kd_fwd_ws(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N,
+                                int64_t Lq, int64_t Ld, int64_t dim, const bool* qmask,
+                                const bool* dmask, float* scores, int32_t* argmax, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
 /*   grad_out [B, N], argmax [B, N, Lq], grad_Q [B, Lq, dim], grad_D [B, N, Ld, dim] */
 lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype,
                              int64_t B, int64_t N, int64_t Lq, int64_t Ld, int64_t dim,
@@ -186,8 +255,8 @@ lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype,
  * The same backward with grad_Q and grad_D in the dtype of Q and D instead of
  * fp32, so a bf16/fp16 training step keeps no fp32 gradient buffers and writes
  * half the bytes (colpali PR "Add support for late-interaction-kernels
- * (LIK)", Results: the fused backward allocates only the input gradients,
- * and its cost is dominated by writing grad_D).  Every element is summed in
+ * (LIK)", Results: the fused backward's memory is the two input gradients,
+ * and writing grad_D is most of its cost).  Every element is summed in
  * fp32 and rounded to the output type once (round to nearest even); each
  * row of grad_D is written exactly once, zeros included.
  *   - fp32 inputs: identical to the fp32 entry points.
@@ -256,7 +325,8 @@ lik_status lik_maxsim_kd_bwd_recompute(const void* Q, const void* D, lik_dtype d
  *   - Nq * Nd * Lq <= 2097152, else LIK_ERR_UNSUPPORTED (nothing launched).
  *   - Nothing is allocated.  The first call on a device, with that device
  *     current, looks up the array's device address (cudaGetSymbolAddress);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture, and do not reset the
+ *     device afterwards (the address is kept for the process's life).
  *   - Every call shares the array; calls whose work overlaps on the GPU
  *     race on it, so order them (one stream, or events).  Its contents need
  *     no clearing: the forward writes every entry the backward reads.

@@ -28,11 +28,16 @@ SIGNATURES = {
     "lik_last_error_message": (ctypes.c_char_p, []),
     "lik_version": (ctypes.c_char_p, []),
     "lik_check_device_error": (_I32, [_P]),
+    "lik_selftest_bounded_wait": (_I32, [_I64, _P]),
     "lik_maxsim_allpairs_fwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_allpairs_bwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_pairwise_fwd": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
     "lik_maxsim_pairwise_bwd": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
     "lik_maxsim_kd_fwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
+    "lik_maxsim_pairwise_fwd_workspace_bytes": (_I32, [_I32] + [_I64] * 4 + [_I32, _P]),
+    "lik_maxsim_kd_fwd_workspace_bytes": (_I32, [_I32] + [_I64] * 5 + [_I32, _P]),
+    "lik_maxsim_pairwise_fwd_ws": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5 + [ctypes.c_size_t, _P]),
+    "lik_maxsim_kd_fwd_ws": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5 + [ctypes.c_size_t, _P]),
     "lik_maxsim_kd_bwd": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_allpairs_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 5 + [_P] * 5),
     "lik_maxsim_pairwise_bwd_same_dtype": (_I32, [_P, _P, _I32] + [_I64] * 4 + [_P] * 5),
@@ -225,6 +230,69 @@ def lik_maxsim_kd_bwd(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=N
         _ptr(grad_Q), _ptr(grad_D), _stream(dev, stream)))
 
 
+# ------------------------------------- caller-provided forward workspace --
+
+def _stream_sizes(kind, Q, D):
+    if kind == "kd":
+        dt, dev = _embeddings(Q, D, 3, 4)
+        B, Lq, dim = Q.shape
+        if D.shape[0] != B:
+            raise ValueError("kd: Q and D must have the same batch size")
+        N, Ld = D.shape[1], D.shape[2]
+        return dt, dev, (B, N, Lq, Ld, dim), (B, N), (B, N, Ld)
+    dt, dev = _embeddings(Q, D, 3, 3)
+    B, Lq, dim = Q.shape
+    if D.shape[0] != B:
+        raise ValueError("pairwise: Q and D must have the same batch size")
+    Ld = D.shape[1]
+    return dt, dev, (B, Lq, Ld, dim), (B,), (B, Ld)
+
+
+def _workspace_bytes(kind, Q, D, has_dmask):
+    dt, dev, sizes, _, _ = _stream_sizes(kind, Q, D)
+    out = ctypes.c_size_t(0)
+    with torch.cuda.device(dev):
+        _check(getattr(load(), f"lik_maxsim_{kind}_fwd_workspace_bytes")(dt, *sizes, 1 if has_dmask else 0,
+                                                                        ctypes.byref(out)))
+    return int(out.value)
+
+
+def lik_maxsim_pairwise_fwd_workspace_bytes(Q, D, has_dmask=True) -> int:
+    """Bytes of device workspace lik_maxsim_pairwise_fwd_ws needs for these inputs."""
+    return _workspace_bytes("pairwise", Q, D, has_dmask)
+
+
+def lik_maxsim_kd_fwd_workspace_bytes(Q, D, has_dmask=True) -> int:
+    """Bytes of device workspace lik_maxsim_kd_fwd_ws needs for these inputs."""
+    return _workspace_bytes("kd", Q, D, has_dmask)
+
+
+def _fwd_ws(kind, Q, D, qmask, dmask, scores, argmax, workspace, stream):
+    dt, dev, sizes, pairs, dshape = _stream_sizes(kind, Q, D)
+    Lq = Q.shape[1]
+    _need(qmask, "qmask", (Q.shape[0], Lq), torch.bool, dev, optional=True)
+    _need(dmask, "dmask", dshape, torch.bool, dev, optional=True)
+    _need(scores, "scores", pairs, torch.float32, dev)
+    _need(argmax, "argmax", (*pairs, Lq), torch.int32, dev, optional=True)
+    if workspace is not None and (workspace.device != dev or not workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(getattr(load(), f"lik_maxsim_{kind}_fwd_ws")(
+        _ptr(Q), _ptr(D), dt, *sizes, _ptr(qmask), _ptr(dmask), _ptr(scores), _ptr(argmax),
+        _ptr(workspace), nbytes, _stream(dev, stream)))
+
+
+def lik_maxsim_pairwise_fwd_ws(Q, D, qmask, dmask, scores, argmax=None, workspace=None, stream=None):
+    """Pairwise forward with a caller-provided workspace (any dtype tensor of at
+    least lik_maxsim_pairwise_fwd_workspace_bytes bytes); allocates nothing."""
+    _fwd_ws("pairwise", Q, D, qmask, dmask, scores, argmax, workspace, stream)
+
+
+def lik_maxsim_kd_fwd_ws(Q, D, qmask, dmask, scores, argmax=None, workspace=None, stream=None):
+    """Per-query-candidate forward with a caller-provided workspace; allocates nothing."""
+    _fwd_ws("kd", Q, D, qmask, dmask, scores, argmax, workspace, stream)
+
+
 # ------------------------------------------- gradients in the inputs' dtype --
 
 def lik_maxsim_allpairs_bwd_same_dtype(Q, D, grad_out, argmax, grad_Q=None, grad_D=None, stream=None):
@@ -394,6 +462,13 @@ def lik_check_device_error(stream=None, device=None):
     """Synchronise the stream and raise if a kernel flagged an error."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _check(load().lik_check_device_error(_stream(dev, stream)))
+
+
+def lik_selftest_bounded_wait(timeout_us: int, stream=None, device=None):
+    """Make one bounded device wait run out (see include/lik.h); the next
+    lik_check_device_error on the stream then raises LIK_ERR_TIMEOUT."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(load().lik_selftest_bounded_wait(int(timeout_us), _stream(dev, stream)))
 
 
 def version() -> str:

@@ -5,8 +5,8 @@
 // late-interaction-kernels (LIK)" describes for its backend (Design section:
 // device capability, embedding size, matching devices), with one difference:
 // an ineligible call returns a status code and never falls back to another
-// backend.  CUDA errors are always propagated (same section: real kernel
-// errors always propagate).
+// backend.  CUDA errors are always propagated (same section: a genuine
+// kernel failure is never hidden behind a fallback).
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
@@ -192,10 +192,20 @@ Problem make_problem(int layout, lik_dtype dtype, const void* Q, const void* D,
     return P;
 }
 
+// A caller's workspace for the streaming forward (caller_ws): NULL is allowed
+// only when the path needs none; otherwise it must be device memory of the
+// current device, 16-byte aligned and at least the needed size.
+struct CallerWorkspace {
+    bool given = false;
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+
 // scores may be NULL only for the backward's recompute (argmax_only): the
 // kernels then write the argmax alone.
 lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float* scores,
-                   int32_t* argmax, cudaStream_t stream, bool argmax_only = false) {
+                   int32_t* argmax, cudaStream_t stream, bool argmax_only = false,
+                   CallerWorkspace ws = CallerWorkspace()) {
     int dev = 0;
     lik_status st = check_device(&dev);
     if (st != LIK_OK) return st;
@@ -220,7 +230,15 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
         e = launch_fwd_tc_allpairs(P, scores, argmax, stream);
         what = "tensor-core all-pairs forward launch";
     } else if (tc_stream_eligible(P)) {
-        e = launch_fwd_tc_stream(P, scores, argmax, stream);
+        if (ws.given) {
+            const size_t need = stream_workspace_bytes(P, dmask != nullptr);
+            if (!ws.ptr || ws.bytes < need)
+                return fail(LIK_ERR_INVALID_ARG, "workspace of %zu bytes given, this call needs %zu", ws.ptr ? ws.bytes : 0,
+                            need);
+            if ((st = check_pointer(ws.ptr, dev, "workspace")) != LIK_OK) return st;
+            if ((st = check_aligned(ws.ptr, 16, "workspace")) != LIK_OK) return st;
+        }
+        e = launch_fwd_tc_stream(P, scores, argmax, ws.given ? ws.ptr : nullptr, ws.bytes, stream);
         what = "tensor-core streaming forward launch";
     } else {
         e = launch_fwd_simt(P, scores, argmax, stream);
@@ -417,6 +435,67 @@ lik_status lik_maxsim_kd_bwd(const void* Q, const void* D, lik_dtype dtype, int6
     Problem P = make_problem(kKd, dtype, Q, D, nullptr, nullptr, B, B * N, N, B * N, Lq, Ld, dim);
     if (nothing) P.n_pairs = 0;
     return run_bwd(P, grad_out, argmax, grad_Q, grad_D, stream);
+}
+
+lik_status lik_maxsim_pairwise_fwd_workspace_bytes(lik_dtype dtype, int64_t B, int64_t Lq, int64_t Ld, int64_t dim,
+                                                  int has_dmask, size_t* bytes) {
+    t_message[0] = 0;
+    if (!bytes) return fail(LIK_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    int dev = 0;
+    if ((st = check_device(&dev)) != LIK_OK) return st;
+    Problem P = make_problem(kPairwise, dtype, nullptr, nullptr, nullptr, nullptr, B, B, 1, B, Lq, Ld, dim);
+    if (tc_stream_eligible(P)) *bytes = stream_workspace_bytes(P, has_dmask != 0);
+    return LIK_OK;
+}
+
+lik_status lik_maxsim_kd_fwd_workspace_bytes(lik_dtype dtype, int64_t B, int64_t N, int64_t Lq, int64_t Ld,
+                                            int64_t dim, int has_dmask, size_t* bytes) {
+    t_message[0] = 0;
+    if (!bytes) return fail(LIK_ERR_INVALID_ARG, "bytes is NULL");
+    *bytes = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    int dev = 0;
+    if ((st = check_device(&dev)) != LIK_OK) return st;
+    Problem P = make_problem(kKd, dtype, nullptr, nullptr, nullptr, nullptr, B, B * N, N, B * N, Lq, Ld, dim);
+    if (tc_stream_eligible(P)) *bytes = stream_workspace_bytes(P, has_dmask != 0);
+    return LIK_OK;
+}
+
+lik_status lik_maxsim_pairwise_fwd_ws(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t Lq,
+                                      int64_t Ld, int64_t dim, const bool* qmask, const bool* dmask,
+                                      float* scores, int32_t* argmax, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B, 1, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kPairwise, dtype, Q, D, qmask, dmask, B, B, 1, B, Lq, Ld, dim);
+    CallerWorkspace ws;
+    ws.given = true;
+    ws.ptr = workspace;
+    ws.bytes = workspace_bytes;
+    return run_fwd(P, qmask, dmask, scores, argmax, stream, false, ws);
+}
+
+lik_status lik_maxsim_kd_fwd_ws(const void* Q, const void* D, lik_dtype dtype, int64_t B, int64_t N, int64_t Lq,
+                                int64_t Ld, int64_t dim, const bool* qmask, const bool* dmask, float* scores,
+                                int32_t* argmax, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, B, B * N, N, Lq, Ld, dim, &nothing);
+    if (st != LIK_OK || nothing) return st;
+    Problem P = make_problem(kKd, dtype, Q, D, qmask, dmask, B, B * N, N, B * N, Lq, Ld, dim);
+    CallerWorkspace ws;
+    ws.given = true;
+    ws.ptr = workspace;
+    ws.bytes = workspace_bytes;
+    return run_fwd(P, qmask, dmask, scores, argmax, stream, false, ws);
 }
 
 lik_status lik_maxsim_allpairs_bwd_same_dtype(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,

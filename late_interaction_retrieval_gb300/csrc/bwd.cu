@@ -12,7 +12,7 @@
 // argmax -1 (masked query token, empty document) contributes nothing.  The
 // backward allocates nothing: it writes the two input gradients only (colpali
 // PR "Add support for late-interaction-kernels (LIK)", Results: the fused
-// backward allocates only the input gradients).  Every saved argmax is
+// backward's memory is the two input gradients and nothing else).  Every saved argmax is
 // checked: an index >= Ld is skipped (never dereferenced) and flagged in the
 // library's error word.
 #include "dtype_load.cuh"

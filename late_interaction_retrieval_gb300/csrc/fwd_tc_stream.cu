@@ -905,10 +905,42 @@ bool tc_stream_eligible(const Problem& P) {
            P.n_doc < (int64_t(1) << 31) && stream_stages(P, device_info(dev).max_smem_optin) >= 2;
 }
 
+// Byte offsets of the forward's schedule and merge workspace (plan outputs
+// with a document mask, then the cut-document merge slots and counters),
+// each 256-byte aligned from the workspace's start.
+struct WsLayout {
+    int64_t tiles, grid, n_groups;
+    size_t o_units, o_groups, o_words, o_pm, o_pa, o_ne, o_arr, bytes;
+};
+
+static WsLayout ws_layout(const Problem& P, bool has_dmask, int sm_count) {
+    WsLayout L{};
+    L.tiles = (P.Ld + kRows - 1) / kRows;
+    const int64_t all_tiles = P.n_pairs * L.tiles;
+    // one CTA per SM, fewer only when there are fewer tiles than SMs
+    L.grid = all_tiles < sm_count ? all_tiles : sm_count;
+    L.n_groups = has_dmask ? (P.n_pairs + 31) / 32 : 0;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = (off + bytes + 255) & ~size_t(255);
+        return at;
+    };
+    L.o_units = take(has_dmask ? static_cast<size_t>(P.n_pairs) * 4 : 0);
+    L.o_groups = take(static_cast<size_t>(L.n_groups) * 4);
+    L.o_words = take(has_dmask ? static_cast<size_t>(all_tiles) * 16 : 0);
+    L.o_pm = take(static_cast<size_t>(2 * L.grid) * 32 * 4);
+    L.o_pa = take(static_cast<size_t>(2 * L.grid) * 32 * 4);
+    L.o_ne = take(static_cast<size_t>(2 * L.grid) * 4);
+    L.o_arr = take(static_cast<size_t>(L.grid) * 4);
+    L.bytes = off;
+    return L;
+}
+
 // Library-owned memory pool of a device for the forward's schedule and merge
-// workspace (a few hundred bytes per CTA plus 4 bytes per pair): allocations
-// are stream-ordered and freed on the stream after the kernel, and the pool
-// keeps the memory it has mapped, so steady-state calls map nothing new.
+// workspace when the caller passes none: allocations are stream-ordered and
+// freed on the stream after the kernel, and the pool keeps the memory it has
+// mapped, so steady-state calls map nothing new.
 static cudaError_t workspace_pool(int dev, cudaMemPool_t* out) {
     static std::mutex mu;
     static std::vector<cudaMemPool_t> pools;
@@ -934,7 +966,14 @@ static cudaError_t workspace_pool(int dev, cudaMemPool_t* out) {
     return cudaSuccess;
 }
 
-cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax, cudaStream_t stream) {
+size_t stream_workspace_bytes(const Problem& P, bool has_dmask) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return ws_layout(P, has_dmask, device_info(dev).sm_count).bytes;
+}
+
+cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -983,39 +1022,29 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
     e = cudaFuncSetAttribute(stream_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    // One CTA per SM, fewer only when there are fewer tiles than SMs.
-    p.tiles = (P.Ld + kRows - 1) / kRows;
-    const int64_t all_tiles = P.n_pairs * p.tiles;
-    const int64_t grid = all_tiles < info.sm_count ? all_tiles : info.sm_count;
-    const int threads = kThreads;
+    const WsLayout L = ws_layout(P, P.dmask != nullptr, info.sm_count);
+    p.tiles = L.tiles;
+    p.n_groups = L.n_groups;
+    const int64_t grid = L.grid;
 
-    // workspace: [units | group_units] (with a document mask) | part_m | part_a | part_ne | arrivals
-    p.n_groups = P.dmask ? (P.n_pairs + 31) / 32 : 0;
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = off;
-        off = (off + bytes + 255) & ~size_t(255);
-        return at;
-    };
-    const size_t o_units = take(P.dmask ? static_cast<size_t>(P.n_pairs) * 4 : 0);
-    const size_t o_groups = take(static_cast<size_t>(p.n_groups) * 4);
-    const size_t o_words = take(P.dmask ? static_cast<size_t>(all_tiles) * 16 : 0);
-    const size_t o_pm = take(static_cast<size_t>(2 * grid) * 32 * 4);
-    const size_t o_pa = take(static_cast<size_t>(2 * grid) * 32 * 4);
-    const size_t o_ne = take(static_cast<size_t>(2 * grid) * 4);
-    const size_t o_arr = take(static_cast<size_t>(grid) * 4);
-    cudaMemPool_t pool = nullptr;
-    if ((e = workspace_pool(dev, &pool)) != cudaSuccess) return e;
-    void* ws = nullptr;
-    if ((e = cudaMallocFromPoolAsync(&ws, off, pool, stream)) != cudaSuccess) return e;
+    // the caller's workspace, or one from the library's pool (freed on the
+    // stream after the kernel)
+    void* ws = workspace;
+    if (ws == nullptr) {
+        cudaMemPool_t pool = nullptr;
+        if ((e = workspace_pool(dev, &pool)) != cudaSuccess) return e;
+        if ((e = cudaMallocFromPoolAsync(&ws, L.bytes, pool, stream)) != cudaSuccess) return e;
+    } else if (workspace_bytes < L.bytes) {
+        return cudaErrorInvalidValue;  // the entry points check the size before calling
+    }
     uint8_t* base = static_cast<uint8_t*>(ws);
-    p.units = P.dmask ? reinterpret_cast<const int32_t*>(base + o_units) : nullptr;
-    p.group_units = P.dmask ? reinterpret_cast<const int32_t*>(base + o_groups) : nullptr;
-    p.words = P.dmask ? reinterpret_cast<const uint4*>(base + o_words) : nullptr;
-    p.part_m = reinterpret_cast<float*>(base + o_pm);
-    p.part_a = reinterpret_cast<int32_t*>(base + o_pa);
-    p.part_ne = reinterpret_cast<int32_t*>(base + o_ne);
-    p.arrivals = reinterpret_cast<unsigned int*>(base + o_arr);
+    p.units = P.dmask ? reinterpret_cast<const int32_t*>(base + L.o_units) : nullptr;
+    p.group_units = P.dmask ? reinterpret_cast<const int32_t*>(base + L.o_groups) : nullptr;
+    p.words = P.dmask ? reinterpret_cast<const uint4*>(base + L.o_words) : nullptr;
+    p.part_m = reinterpret_cast<float*>(base + L.o_pm);
+    p.part_a = reinterpret_cast<int32_t*>(base + L.o_pa);
+    p.part_ne = reinterpret_cast<int32_t*>(base + L.o_ne);
+    p.arrivals = reinterpret_cast<unsigned int*>(base + L.o_arr);
 
     PlanArgs pa{};
     pa.dmask = P.dmask;
@@ -1023,11 +1052,12 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
     pa.Ld = P.Ld;
     pa.tiles = p.tiles;
     pa.n_groups = p.n_groups;
-    pa.units = reinterpret_cast<int32_t*>(base + o_units);
-    pa.group_units = reinterpret_cast<int32_t*>(base + o_groups);
-    pa.words = reinterpret_cast<uint4*>(base + o_words);
+    pa.units = reinterpret_cast<int32_t*>(base + L.o_units);
+    pa.group_units = reinterpret_cast<int32_t*>(base + L.o_groups);
+    pa.words = reinterpret_cast<uint4*>(base + L.o_words);
     pa.arrivals = p.arrivals;
     pa.n_arrivals = grid;
+    const int64_t all_tiles = P.n_pairs * p.tiles;
     const int64_t word_blocks = P.dmask ? (all_tiles + 255) / 256 : 0;
     const int64_t zero_blocks = (grid + 1023) / 1024;
     const int64_t plan_blocks =
@@ -1037,7 +1067,7 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
     if (e == cudaSuccess) {
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(threads);
+        cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
@@ -1047,8 +1077,11 @@ cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argma
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, stream_fwd_tc_kernel, tmq, tmd, p);
     }
-    const cudaError_t ef = cudaFreeAsync(ws, stream);
-    return e != cudaSuccess ? e : ef;
+    if (workspace == nullptr) {
+        const cudaError_t ef = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess) e = ef;
+    }
+    return e;
 }
 
 }  // namespace lik

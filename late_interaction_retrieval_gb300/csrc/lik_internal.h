@@ -75,10 +75,14 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
                                    cudaStream_t stream);
 
 // Tensor-core (tcgen05) streaming forward for the pairwise and kd layouts,
-// fp16/bf16: dim % 16 == 0, dim <= 256, 1 <= Lq <= 32, Ld >= 1.
+// fp16/bf16: dim % 16 == 0, dim <= 256, 1 <= Lq <= 32, Ld >= 1.  It needs a
+// device workspace of stream_workspace_bytes(P, P.dmask != nullptr) bytes
+// (16-byte aligned): the caller's, or, with workspace == nullptr, one from
+// the library's pool.
 bool tc_stream_eligible(const Problem& P);
-cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax,
-                                 cudaStream_t stream);
+size_t stream_workspace_bytes(const Problem& P, bool has_dmask);
+cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
 
 // Backward: grad_Q gather and grad_D scatter (grad_D zero-filled first).
 cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,

@@ -66,17 +66,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // pipeline ends the kernel instead of hanging the GPU.
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;  // 2 s; a healthy wait takes microseconds
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, unsigned int* err,
+                                              uint64_t timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
 #pragma unroll 1
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+        if (globaltimer_ns() - t0 > timeout_ns) {
             atomicOr(err, kErrTimeout);
             return false;
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned int* err) {
+    return mbar_wait_for(bar, parity, err, kWaitTimeoutNs);
 }
 
 // ------------------------------------------------------------------ TMA --

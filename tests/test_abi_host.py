@@ -90,3 +90,19 @@ def test_message_cleared_on_next_call(lib):
     assert lib.lik_last_error_message().decode() != ""
     assert _fwd(lib, Nq=0) == 0
     assert lib.lik_last_error_message().decode() == ""
+
+
+def test_selftest_timeout_range(lib):
+    assert lib.lik_selftest_bounded_wait(0, NULL) == 1
+    assert lib.lik_selftest_bounded_wait(1000001, NULL) == 1
+    assert "timeout_us" in lib.lik_last_error_message().decode()
+
+
+def test_workspace_query_rejects_bad_arguments(lib):
+    assert lib.lik_maxsim_pairwise_fwd_workspace_bytes(2, 4, 32, 100, 128, 1, NULL) == 1
+    import ctypes
+    out = ctypes.c_size_t(7)
+    assert lib.lik_maxsim_kd_fwd_workspace_bytes(2, -1, 3, 32, 100, 128, 1, ctypes.byref(out)) == 1
+    assert out.value == 0
+    assert lib.lik_maxsim_kd_fwd_workspace_bytes(2, 0, 3, 32, 100, 128, 1, ctypes.byref(out)) == 0
+    assert out.value == 0
