@@ -10,6 +10,12 @@ metric counts 2*Nq*Nd*Lq*Ld*dim FLOPs (padded Ld) per step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, as it stands
 
+The line also carries "roofline_bwd" (each backward kernel timed on its own,
+with the bytes it must move) and, in a single-GPU run of the default step,
+"configs": one record per other workload (per-query candidates fwd+bwd,
+long-document reranking fwd, large all-pairs inference fwd), each measured
+the same way, with its own roofline, clocks and CPU-oracle sample.
+
 Under torchrun (N > 1) every rank runs an independent replica of the
 workload (weak scaling, no collective on the data path); timings are
 max-reduced over ranks and rank 0 prints one JSON line.
@@ -276,18 +282,16 @@ class Step:
 
 # ---------------------------------------------------------------- our arm --
 
-def run_ours(args):
-    world, rank, local = dist_env()
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    name = args.workload
-    st = Step(name, device, args.grad_dtype, ce=args.step == "ce", recompute=args.step == "recompute")
+# Workloads measured after the headline one in a default single-GPU run, each
+# as one record of the line's "configs" object.
+EXTRA_WORKLOADS = ("kd_b256_n17_bf16", "rerank_b512_ld8192_f16", "allpairs_q128_d4096_bf16")
+
+
+def timed_steps(st: Step, args, stream, flush, world):
+    """Warm-up steps, then `args.steps` device-timed steps (CUDA events on the
+    launching stream, L2 flushed between steps), with the SM clocks sampled
+    while they run (identical untimed steps extend the load to >= 1 s)."""
     w = st.w
-    stream = torch.cuda.current_stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
     def one_step():
         st.fwd()
@@ -299,11 +303,9 @@ def run_ours(args):
         one_step()
     torch.cuda.synchronize()
     st.binding.lik_check_device_error()
-
-    # ---- device-timed steps, inputs resident in HBM, L2 flushed in between
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(device).start()
+    sampler = ClockSampler(st.device).start()
     time.sleep(0.15)
     if world > 1:
         torch.distributed.barrier()
@@ -320,7 +322,6 @@ def run_ours(args):
         e2.record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
-    # keep the same load until the clock sampler has seen >= 1 s of it
     while time.perf_counter() - t_wall0 < 1.0:
         for _ in range(20):
             flush.zero_()
@@ -328,67 +329,196 @@ def run_ours(args):
         torch.cuda.synchronize()
     clocks = sampler.stop()
     st.binding.lik_check_device_error()
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
-    total_ms = max_over_ranks(sum(step_ms), device)
+    return {"step_ms": [a.elapsed_time(c) for a, _, c in ev],
+            "fwd_ms": [a.elapsed_time(b) for a, b, _ in ev], "clocks": clocks, "wall_s": t_wall}
+
+
+def forward_roofline(st: Step, name: str, fwd_avg_ms: float, peaks) -> dict:
+    """Roofline of the step's forward kernel(s), from their CUDA-event time."""
+    w = st.w
+    if w.layout in ("pairwise", "kd"):
+        kernel = "stream_fwd_tc_kernel"
+        units = st.algorithmic_bytes()
+        roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "algorithmic_bytes": units}
+    else:
+        kernel = "allpairs_fwd_tc_kernel"
+        roof = {"bound": "tensor", "achieved": w.counted_flops / (fwd_avg_ms * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(kernel, name)
+    roof["kernel"] = kernel
+    roof["peak_source"] = f"{peaks['source']} (burst; kernel timed alone within a short step)"
+    if roof["bound"] == "tensor":
+        roof["frac_of_sustained"] = roof["achieved"] / peaks["bf16_tflops_sustained"]
+    roof["kernel_ms"] = fwd_avg_ms
+    return roof
+
+
+def backward_roofline(st: Step, args, stream, flush, peaks) -> dict:
+    """Each backward kernel timed on its own (the entry point called with only
+    grad_Q, then only grad_D), with the bytes it must move.
+
+    grad_Q gathers one document row per (pair, query token) hit; grad_D
+    zero-fills grad_D (fp32 gradients) and adds one Q row per hit into it.
+    `dram_bytes` is what the kernel must move to or from DRAM at least
+    (argmax, upstream gradient, its output, the distinct rows it reads);
+    `l2_bytes` is the row traffic it makes (gathers, or reductions into
+    grad_D), served by L2 where the rows are resident.
+    """
+    w, i = st.w, st.inp
+    el = i.Q.element_size()
+    gel = st.gQ.element_size()
+    hits = int((st.argmax >= 0).sum())
+    pairs = st.argmax.numel() // w.lq
+    am_bytes, g_bytes = st.argmax.numel() * 4, pairs * 4
+    d_bytes = i.D.numel() * el
+    fn = getattr(st.binding, f"lik_maxsim_{w.layout}_bwd" + ("_same_dtype" if st.same_dtype else ""))
+
+    def time_it(gq, gd):
+        for _ in range(3):
+            flush.zero_()
+            fn(i.Q, i.D, st.g, st.argmax, gq, gd)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            fn(i.Q, i.D, st.g, st.argmax, gq, gd)
+            b.record(stream)
+        torch.cuda.synchronize()
+        st.binding.lik_check_device_error()
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    ms_q = time_it(st.gQ, None)
+    ms_d = time_it(None, st.gD)
+    gathered = hits * w.dim * el
+    q_dram = am_bytes + g_bytes + st.gQ.numel() * gel + min(gathered, d_bytes)
+    resident = d_bytes < (96 << 20)  # rows fit in L2 next to everything else
+    gq = {"kernel": "grad_q_vec_kernel", "ms": ms_q, "hits": hits, "l2_bytes": gathered,
+          "l2_gbs": gathered / (ms_q * 1e-3) / 1e9, "dram_bytes": q_dram,
+          "achieved": q_dram / (ms_q * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+          "bound": "l2 (gathered document rows are L2-resident)" if resident else "hbm"}
+    gq["frac"] = gq["achieved"] / gq["peak"]
+    red_bytes = hits * w.dim * 4
+    gd_out = st.gD.numel() * gel
+    d_dram = am_bytes + g_bytes + i.Q.numel() * el + gd_out
+    kernel_d = "grad_d_scatter_vec_kernel (after a zero-fill of grad_D)" if not st.same_dtype else \
+        "grad_d (one write per row, inputs' dtype)"
+    gd = {"kernel": kernel_d, "ms": ms_d, "hits": hits, "l2_bytes": red_bytes if not st.same_dtype else hits * w.dim * el,
+          "reductions": hits * (w.dim // 4) if not st.same_dtype else 0,
+          "dram_bytes": d_dram, "achieved": d_dram / (ms_d * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+          "bound": ("l2 (16-byte fp32 reductions into grad_D)" if resident else "hbm (grad_D write)")
+          if not st.same_dtype else "hbm (grad_D write)"}
+    gd["l2_gbs"] = gd["l2_bytes"] / (ms_d * 1e-3) / 1e9
+    gd["frac"] = gd["achieved"] / gd["peak"]
+    return {"grad_q": gq, "grad_d": gd}
+
+
+def config_record(name: str, device, args, stream, flush, peaks) -> dict:
+    """One extra workload measured like the headline one (same steps, L2
+    flush and clock sampling), as a record of the line's "configs"."""
+    st = Step(name, device, "f32")
+    w = st.w
+    t = timed_steps(st, args, stream, flush, 1)
+    ms = statistics.mean(t["step_ms"])
+    fwd_ms = statistics.mean(t["fwd_ms"])
+    if w.layout == "pairwise" and not w.backward:
+        value, unit = st.algorithmic_bytes() / (ms * 1e-3) / 1e9, "GB/s"
+    else:
+        value, unit = w.counted_flops / (ms * 1e-3) / 1e12, "TFLOP/s"
+    rec = {"workload": name, "layout": w.layout, "Q": list(w.q_shape), "D": list(w.d_shape), "dtype": w.dtype,
+           "passes": "fwd+bwd" if w.backward else "fwd", "value": value, "unit": unit, "ms_per_step": ms,
+           "fwd_ms": fwd_ms, "steps": args.steps, "counted_flops_per_step": w.counted_flops,
+           "valid_token_flops_per_step": st.valid_flops(), "algorithmic_fwd_bytes": st.algorithmic_bytes(),
+           "roofline": forward_roofline(st, name, fwd_ms, peaks), "clocks": t["clocks"],
+           "gpu_launches": st.launches_per_step * args.steps}
+    if w.backward:
+        rec["grad_dtype"] = "f32"
+        rec["roofline_bwd"] = backward_roofline(st, args, stream, flush, peaks)
+    del st
+    torch.cuda.empty_cache()
+    if not args.no_cpu_baseline:
+        rec["cpu_baseline"] = cpu_baseline(name, unit, budget_s=4.0)
+    return rec
+
+
+def run_ours(args):
+    world, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    name = args.workload
+    st = Step(name, device, args.grad_dtype, ce=args.step == "ce", recompute=args.step == "recompute")
+    w = st.w
+    stream = torch.cuda.current_stream(device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    peaks = measured_peaks()
+
+    # ---- device-timed steps, inputs resident in HBM, L2 flushed in between
+    t = timed_steps(st, args, stream, flush, world)
+    total_ms = max_over_ranks(sum(t["step_ms"]), device)
+    fwd_avg_ms = statistics.mean(t["fwd_ms"])
 
     # ---- end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(st, args, stream, world)
 
+    # ---- each backward kernel on its own (plain fwd+bwd steps)
+    bwd_roof = None
+    if w.backward and not st.ce and not st.recompute:
+        bwd_roof = backward_roofline(st, args, stream, flush, peaks)
+
+    fwd_bytes_step = st.algorithmic_bytes()
+    roof = forward_roofline(st, name, fwd_avg_ms, peaks)
+    config = {
+        "workload": name, "layout": w.layout,
+        "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
+        "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
+        "loss_head": "cross-entropy inside the step" if st.ce else "score gradient precomputed",
+        "argmax": ("recomputed in the backward" if st.recompute else "saved by the forward")
+                  if w.backward else None,
+        "counted_flops_per_step": w.counted_flops, "valid_token_flops_per_step": st.valid_flops(),
+        "algorithmic_fwd_bytes": fwd_bytes_step,
+        "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        "fwd_ms": fwd_avg_ms, "wall_s": t["wall_s"],
+    }
+    launches = st.launches_per_step * args.steps
+
+    # ---- the other workloads, one record each (single GPU, default step only)
+    configs = None
+    if world == 1 and not args.no_extra_configs and args.step == "fwd+bwd" and args.grad_dtype == "f32":
+        del st
+        torch.cuda.empty_cache()
+        configs = {n: config_record(n, device, args, stream, flush, peaks) for n in EXTRA_WORKLOADS if n != name}
+
     if rank == 0:
-        peaks = measured_peaks()
         ms_per_step = total_ms / args.steps
-        fwd_avg_ms = statistics.mean(fwd_ms)
-        counted = w.counted_flops
-        fwd_only_pairwise = (w.layout == "pairwise" and not w.backward)
-        if fwd_only_pairwise:
-            units = st.algorithmic_bytes()
-            value = whole_job_rate(world, args.steps, units, total_ms, 1e9)
+        if w.layout == "pairwise" and not w.backward:
+            value = whole_job_rate(world, args.steps, fwd_bytes_step, total_ms, 1e9)
             unit = "GB/s"
-            roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9,
-                    "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-            kernel = "stream_fwd_tc_kernel"
         else:
-            value = whole_job_rate(world, args.steps, counted, total_ms, 1e12)
+            value = whole_job_rate(world, args.steps, w.counted_flops, total_ms, 1e12)
             unit = "TFLOP/s"
-            kernel = "allpairs_fwd_tc_kernel" if w.layout == "allpairs" else "stream_fwd_tc_kernel"
-            if w.layout == "kd":
-                units = st.algorithmic_bytes()
-                roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9,
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-            else:
-                roof = {"bound": "tensor", "achieved": counted / (fwd_avg_ms * 1e-3) / 1e12,
-                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-        roof["frac"] = roof["achieved"] / roof["peak"]
-        roof["traffic"] = kernel_traffic(kernel, name)
-        roof["kernel"] = kernel
-        roof["peak_source"] = f"{peaks['source']} (burst; kernel timed alone within a short step)"
-        roof["kernel_ms"] = fwd_avg_ms
         cpu = cpu_baseline(name, unit) if not args.no_cpu_baseline else None
         line = {
             "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded, L2-normalised Gaussian tokens)",
-            "config": {
-                "workload": name, "layout": w.layout,
-                "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
-                "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
-                "loss_head": "cross-entropy inside the step" if st.ce else "score gradient precomputed",
-                "argmax": ("recomputed in the backward" if st.recompute else "saved by the forward")
-                          if w.backward else None,
-                "counted_flops_per_step": counted, "valid_token_flops_per_step": st.valid_flops(),
-                "algorithmic_fwd_bytes": st.algorithmic_bytes(),
-                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write)",
-                "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                "fwd_ms": fwd_avg_ms, "wall_s": t_wall,
-            },
+            "config": config,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": st.launches_per_step * args.steps,
-            "clocks": clocks,
+            "gpu_launches": launches,
+            "clocks": t["clocks"],
         }
+        if bwd_roof is not None:
+            line["roofline_bwd"] = bwd_roof
+        if configs:
+            line["configs"] = configs
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -500,8 +630,8 @@ def oracle_sample(name: str, budget_s: float, max_steps: int | None = None):
     return results, orc.num_threads(), desc
 
 
-def cpu_baseline(name: str, unit: str):
-    results, cores, desc = oracle_sample(name, budget_s=12.0)
+def cpu_baseline(name: str, unit: str, budget_s: float = 12.0):
+    results, cores, desc = oracle_sample(name, budget_s=budget_s)
     secs = sum(r[0] for r in results)
     flops = sum(r[1] for r in results)
     w = W.WORKLOADS[name]
@@ -562,6 +692,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="inbatch_b128_bf16", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-configs", action="store_true",
+                    help="measure only --workload (by default a single-GPU run of the default step also "
+                         "measures the per-query-candidate, reranking and large all-pairs workloads)")
     ap.add_argument("--step", choices=["fwd+bwd", "ce", "recompute"], default="fwd+bwd",
                     help="ce: the workload's cross-entropy head (loss and score gradient) inside every step; "
                          "recompute: the forward saves no argmax and the backward recomputes it")
