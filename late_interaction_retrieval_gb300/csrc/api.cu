@@ -240,6 +240,9 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
         }
         e = launch_fwd_tc_stream(P, scores, argmax, ws.given ? ws.ptr : nullptr, ws.bytes, stream);
         what = "tensor-core streaming forward launch";
+    } else if (tc_f32_eligible(P)) {
+        e = launch_fwd_tc_f32(P, scores, argmax, stream);
+        what = "tensor-core fp32 (split TF32) forward launch";
     } else {
         e = launch_fwd_simt(P, scores, argmax, stream);
         what = "forward launch";

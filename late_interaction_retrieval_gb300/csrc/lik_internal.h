@@ -84,6 +84,11 @@ size_t stream_workspace_bytes(const Problem& P, bool has_dmask);
 cudaError_t launch_fwd_tc_stream(const Problem& P, float* scores, int32_t* argmax, void* workspace,
                                  size_t workspace_bytes, cudaStream_t stream);
 
+// Tensor-core (tcgen05 kind::tf32, three-product hi/lo split) forward for
+// fp32 inputs, every layout: dim % 8 == 0, dim <= 128, 1 <= Lq <= 128, Ld >= 1.
+bool tc_f32_eligible(const Problem& P);
+cudaError_t launch_fwd_tc_f32(const Problem& P, float* scores, int32_t* argmax, cudaStream_t stream);
+
 // Backward: grad_Q gather and grad_D scatter (grad_D zero-filled first).
 cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,
                               const int32_t* argmax, float* grad_Q, cudaStream_t stream);

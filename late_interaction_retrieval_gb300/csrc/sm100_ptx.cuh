@@ -146,6 +146,31 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, fp32 accumulate, TF32 inputs
+// (32-bit containers; the MMA reads the 19 TF32 bits).
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]^T, fp32 accumulate, TF32 inputs, with
+// A (M rows) read from tensor memory: row m in lane m, one TF32 per 32-bit
+// column, the K-step's 8 columns starting at `a_tmem`.
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -189,6 +214,48 @@ __device__ __forceinline__ void mma_kchain(uint32_t d_tmem, uint32_t a_base, uin
                     sw128_kmajor_desc(b_base + atom * b_atom + off), idesc, k != 0);
         }
     }
+}
+
+// The same chain for TF32 operands: K = 8 per instruction, so a k-step is
+// again 32 bytes of a 128-byte row (4 per swizzle atom of 32 fp32).  With
+// `acc_first` the first step accumulates too (a later product of a split).
+template <int kMaxK>
+__device__ __forceinline__ void mma_tf32_kchain(uint32_t d_tmem, uint32_t a_base, uint32_t a_atom, uint32_t b_base,
+                                                uint32_t b_atom, int nk, uint32_t idesc, bool acc_first) {
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < nk) {
+            const uint32_t off = static_cast<uint32_t>(k & 3) * 32;
+            const uint32_t atom = static_cast<uint32_t>(k >> 2);
+            mma_tf32(d_tmem, sw128_kmajor_desc(a_base + atom * a_atom + off),
+                     sw128_kmajor_desc(b_base + atom * b_atom + off), idesc, acc_first || k != 0);
+        }
+    }
+}
+
+// The same chain with A in tensor memory (columns a_col + 8k for k-step k).
+template <int kMaxK>
+__device__ __forceinline__ void mma_tf32_ts_kchain(uint32_t d_tmem, uint32_t a_col, uint32_t b_base, uint32_t b_atom,
+                                                   int nk, uint32_t idesc, bool acc_first) {
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) {
+        if (k < nk) {
+            const uint32_t off = static_cast<uint32_t>(k & 3) * 32;
+            const uint32_t atom = static_cast<uint32_t>(k >> 2);
+            mma_tf32_ts(d_tmem, a_col + 8u * static_cast<uint32_t>(k), sw128_kmajor_desc(b_base + atom * b_atom + off),
+                        idesc, acc_first || k != 0);
+        }
+    }
+}
+
+// Instruction descriptor of tcgen05.mma .kind::tf32: fp32 accumulator, A and
+// B TF32 (format code 2), both K-major, M x N.
+__host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
+    return (1u << 4)                                   // D format: f32
+           | (2u << 7)                                 // A format: tf32
+           | (2u << 10)                                // B format: tf32
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
 // Instruction descriptor of tcgen05.mma .kind::f16: fp32 accumulator,
@@ -252,6 +319,37 @@ __device__ __forceinline__ void tmem_ld_16x2(uint32_t ta, uint32_t tb, uint32_t 
         : "r"(ta), "r"(tb)
         : "memory");
 }
+
+// Two 32-column loads of this thread's lane in flight together, one wait.
+__device__ __forceinline__ void tmem_ld_32x2(uint32_t ta, uint32_t tb, uint32_t (&a)[32], uint32_t (&b)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+        "%28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, "
+        "%42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, "
+        "%60, %61, %62, %63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : LIK_TMEM_LD_X32_OUT(a), LIK_TMEM_LD_X32_OUT(b)
+        : "r"(ta), "r"(tb)
+        : "memory");
+}
+
+// Store 32 consecutive 32-bit columns of this thread's lane (warp-wide; the
+// warp's lanes are its TMEM lane quarter).  Completion: tmem_wait_st().
+__device__ __forceinline__ void tmem_st_32(uint32_t taddr, const uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, "
+        "%31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // tcgen05.ld.red (sm_103a): the 16 columns as tmem_ld_16 returns them, and
 // in `mx` their maximum (IEEE max; +0 over -0), computed by the load.

@@ -47,8 +47,9 @@ bool encode_tmap_kmajor(CUtensorMap* map, int dtype, const void* base, int rank,
         bdim[i] = box[i];
     }
     for (int i = 0; i + 1 < rank; ++i) gstride[i] = strides_bytes[i];
-    const CUtensorMapDataType t =
-        dtype == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUtensorMapDataType t = dtype == kBF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : dtype == kF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUresult r = fn(map, t, static_cast<cuuint32_t>(rank), const_cast<void*>(base), gdim, gstride,
                     bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -9,7 +9,7 @@
 
 namespace lik {
 
-// Encode a tiled tensor map over fp16/bf16 data of rank 2 or 3 with the
+// Encode a tiled tensor map over fp16/bf16/fp32 data of rank 2 or 3 with the
 // 128-byte swizzle; dims are innermost first, strides (rank-1 of them) in
 // bytes for dims 1.., box in elements.  Out-of-bounds box elements read as
 // zero.  Returns false if the driver entry point is unavailable or rejects

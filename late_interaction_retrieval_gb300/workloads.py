@@ -90,6 +90,11 @@ WORKLOADS = {
         "in-batch contrastive all-pairs fwd+bwd, bf16: Q[128,32,128] x "
         "D[128,1030,128]; doc lengths U[700,1030]; grad_out from row-wise "
         "cross-entropy with the diagonal as target"),
+    "inbatch_b128_f32": Workload(
+        "inbatch_b128_f32", "allpairs", 128, 128, 32, 1030, 128, "f32", 5, True,
+        "in-batch contrastive all-pairs fwd+bwd, fp32 inputs: the in-batch recipe "
+        "(Q[128,32,128] x D[128,1030,128], doc lengths U[700,1030], cross-entropy "
+        "score gradient) without rounding the tokens to 16 bits"),
     "kd_b256_n17_bf16": Workload(
         "kd_b256_n17_bf16", "kd", 256, 17, 32, 1030, 128, "bf16", 2, True,
         "per-query candidates fwd+bwd, bf16: Q[256,32,128] x D[256,17,1030,128]; "
@@ -180,7 +185,7 @@ def generate(name: str, device="cpu") -> Inputs:
         qmask = torch.ones((w.nq, w.lq), dtype=torch.bool, device=device)
         qmask[3, 28:] = False
         grad_out = torch.randn(w.score_shape, generator=gen, device=device, dtype=torch.float32)
-    elif name == "inbatch_b128_bf16":
+    elif name in ("inbatch_b128_bf16", "inbatch_b128_f32"):
         dlen = lengths(gen, w.nd, 700, 1030, device)
         dmask = prefix_mask(dlen, w.ld)
         qmask = torch.ones((w.nq, w.lq), dtype=torch.bool, device=device)

@@ -106,6 +106,33 @@ def test_random_sweep(case, dtype):
     h.check_backward(am_oracle=f["am_oracle"])
 
 
+F32_TC_CASES = [
+    # layout,     nq, nd, lq,  ld,  dim   (fp32 inputs on the split-TF32 tensor-core kernel)
+    ("allpairs",   3,  4,  1,   65,   8),  # one K step, one query token
+    ("allpairs",   5,  3, 127, 130,  24),  # Lq = 127: one query per row block, a partial atom
+    ("allpairs",   2,  5, 128,  64,  40),
+    ("allpairs",   9,  6, 33,  200, 120),  # 3 queries per row block, 4 atoms (the last partial)
+    ("allpairs",  37,  3, 16,  129, 128),  # 8 queries per row block, a partial last row block
+    ("allpairs",   1, 300, 32,  70, 128),  # many documents per work unit
+    ("pairwise",   6,  0, 128, 500,  64),
+    ("kd",         3,  7, 20,  333,  96),
+    ("allpairs",   2,  3, 129,  40,  64),  # Lq > 128: the FFMA kernel
+]
+
+
+@pytest.mark.parametrize("case", F32_TC_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_f32_tensor_core_shapes(case):
+    """fp32 inputs at the bar of 1e-5 through the split-TF32 tensor-core
+    forward: embedding sizes from one K step to 128, query lengths up to 128,
+    partial row blocks and atoms, empty documents, all three layouts."""
+    layout, nq, nd, lq, ld, dim = case
+    inp = random_case(layout, nq, nd, lq, ld, dim, "f32", seed=zlib.crc32(repr(case).encode()) % 10_000,
+                      p_doc_empty=0.15)
+    h = gpu_harness.Layout(inp)
+    f = h.check_forward()
+    h.check_backward(am_oracle=f["am_oracle"])
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_odd_dims_simt(dtype):
     """Embedding sizes that are not multiples of 16 still compute exactly."""
