@@ -13,7 +13,8 @@ metric counts 2*Nq*Nd*Lq*Ld*dim FLOPs (padded Ld) per step.
 The line also carries "roofline_bwd" (each backward kernel timed on its own,
 with the bytes it must move) and, in a single-GPU run of the default step,
 "configs": one record per other workload (per-query candidates fwd+bwd,
-long-document reranking fwd, large all-pairs inference fwd), each measured
+long-document reranking fwd, large all-pairs inference fwd, and the in-batch
+workload with fp32 inputs fwd+bwd), each measured
 the same way, with its own roofline, clocks and CPU-oracle sample.
 
 Under torchrun (N > 1) every rank runs an independent replica of the
@@ -49,6 +50,7 @@ _CSRC = "late_interaction_retrieval_gb300/csrc/"
 KERNEL_SOURCES = {
     "allpairs_fwd_tc_kernel": (_CSRC + "fwd_tc_allpairs.cu", _CSRC + "sm100_ptx.cuh", _CSRC + "lik_internal.h"),
     "stream_fwd_tc_kernel": (_CSRC + "fwd_tc_stream.cu", _CSRC + "sm100_ptx.cuh", _CSRC + "lik_internal.h"),
+    "allpairs_fwd_tf32_kernel": (_CSRC + "fwd_tc_f32.cu", _CSRC + "sm100_ptx.cuh", _CSRC + "lik_internal.h"),
 }
 
 
@@ -284,7 +286,10 @@ class Step:
 
 # Workloads measured after the headline one in a default single-GPU run, each
 # as one record of the line's "configs" object.
-EXTRA_WORKLOADS = ("kd_b256_n17_bf16", "rerank_b512_ld8192_f16", "allpairs_q128_d4096_bf16")
+EXTRA_WORKLOADS = ("kd_b256_n17_bf16", "rerank_b512_ld8192_f16", "allpairs_q128_d4096_bf16", "inbatch_b128_f32")
+# nominal dense TF32 / BF16 tensor rates (1.1 / 2.25 PFLOP/s): the fp32 forward
+# runs on TF32 tensor cores, three products per similarity
+TF32_PER_BF16 = 1.1 / 2.25
 
 
 def timed_steps(st: Step, args, stream, flush, world):
@@ -341,6 +346,13 @@ def forward_roofline(st: Step, name: str, fwd_avg_ms: float, peaks) -> dict:
         units = st.algorithmic_bytes()
         roof = {"bound": "hbm", "achieved": units / (fwd_avg_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "algorithmic_bytes": units}
+    elif w.dtype == "f32":
+        kernel = "allpairs_fwd_tf32_kernel"
+        achieved = w.counted_flops / (fwd_avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"] * TF32_PER_BF16,
+                "unit": "TFLOP/s", "peak_dtype": "tf32 (measured bf16 burst x nominal tf32/bf16 ratio)",
+                "tensor_flops_per_counted_flop": 3}
+        roof["tensor_work_frac"] = 3 * achieved / roof["peak"]
     else:
         kernel = "allpairs_fwd_tc_kernel"
         roof = {"bound": "tensor", "achieved": w.counted_flops / (fwd_avg_ms * 1e-3) / 1e12,
@@ -349,7 +361,7 @@ def forward_roofline(st: Step, name: str, fwd_avg_ms: float, peaks) -> dict:
     roof["traffic"] = kernel_traffic(kernel, name)
     roof["kernel"] = kernel
     roof["peak_source"] = f"{peaks['source']} (burst; kernel timed alone within a short step)"
-    if roof["bound"] == "tensor":
+    if roof["bound"] == "tensor" and w.dtype != "f32":
         roof["frac_of_sustained"] = roof["achieved"] / peaks["bf16_tflops_sustained"]
     roof["kernel_ms"] = fwd_avg_ms
     return roof
