@@ -105,6 +105,7 @@ struct Bars {
 
 // What the epilogue hands to the reducers at a document's end, per slot.
 struct Exchange {
+    int stage_seq[kMaxStages];            // tile (index in the CTA's sequence) each D stage holds
     float m[kSlots][kEpiGroups][kM];      // each warpgroup's max per accumulator row
     int a[kSlots][kEpiGroups][kM];        // and its column (-1: none)
     uint32_t any[kSlots][kEpiGroups][4];  // the warpgroup saw a valid column (per warp quarter)
@@ -283,7 +284,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 if (++qb == 2) { qb = 0; qph ^= 1; }
                 return true;
             };
-            int64_t u = blockIdx.x;
+            int64_t u = blockIdx.x, kseq = 0;
             if (u < p.n_units) ok = issue_q(u);
             for (; ok && u < p.n_units; u += gridDim.x) {
                 const int64_t d0 = (u / p.n_rb) * p.dpu;
@@ -298,6 +299,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 for (int64_t d = d0; ok && d < d1; ++d) {
                     for (int t = 0; t < p.tiles_per_doc; ++t) {
                         if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->empty_d[s]), ph ^ 1, err))) break;
+                        xc->stage_seq[s] = static_cast<int>(kseq++);  // published by the arrive below
                         const uint32_t fd = ptx::smem_u32(&bars->full_d[s]);
                         ptx::mbar_arrive_expect_tx(fd, p.d_bytes);
                         for (int a = 0; a < p.atoms; ++a)
@@ -346,6 +348,15 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                     for (int t = 0; t < p.tiles_per_doc; ++t, ++k) {
                         if ((k & 1) == who) {
                             if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph, err))) break;
+                            // With an odd stage count the stage's previous phase belongs to the
+                            // other issuer's tile; if that load is still in flight (loads may
+                            // complete out of order), the parity wait above has passed on it.
+                            // The stage then still names the earlier tile: wait for that phase,
+                            // then for this one.
+                            if (xc->stage_seq[s] != static_cast<int>(k)) {
+                                if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph ^ 1, err))) break;
+                                if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->full_d[s]), ph, err))) break;
+                            }
                             if (!(ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_empty[ab]), aph ^ 1, err))) break;
                             ptx::tc_fence_after();
                             const uint32_t daddr = ptx::smem_u32(dbuf + s * p.d_bytes);
