@@ -251,8 +251,17 @@ lik_status run_fwd(const Problem& P, const bool* qmask, const bool* dmask, float
     return LIK_OK;
 }
 
+// The cross-entropy head of a one-call step, computed inside the grad_Q
+// launch (grad_out is then its score gradient, written there).
+struct FusedCe {
+    const float* scores;
+    const int32_t* target;
+    float scale;
+    float* row_loss;
+};
+
 lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argmax, float* grad_Q,
-                   float* grad_D, cudaStream_t stream) {
+                   float* grad_D, cudaStream_t stream, const FusedCe* ce = nullptr) {
     int dev = 0;
     lik_status st = check_device(&dev);
     if (st != LIK_OK) return st;
@@ -275,8 +284,13 @@ lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argma
     if ((st = check_aligned(grad_Q, 16, "grad_Q")) != LIK_OK) return st;
     if ((st = check_aligned(grad_D, 16, "grad_D")) != LIK_OK) return st;
     cudaError_t e;
-    if (grad_Q && (e = launch_bwd_grad_q(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess)
+    if (ce) {
+        e = launch_bwd_grad_q_ce(P, ce->scores, ce->target, ce->scale, ce->row_loss,
+                                 const_cast<float*>(grad_out), argmax, grad_Q, false, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "grad_Q launch (with the loss head)");
+    } else if (grad_Q && (e = launch_bwd_grad_q(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess) {
         return cuda_fail(e, "grad_Q launch");
+    }
     if (grad_D && (e = launch_bwd_grad_d(P, grad_out, argmax, grad_D, stream)) != cudaSuccess)
         return cuda_fail(e, "grad_D launch");
     return LIK_OK;
@@ -285,9 +299,9 @@ lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argma
 // Backward with grad_Q / grad_D in the inputs' dtype.  fp32 inputs take the
 // fp32 path unchanged.
 lik_status run_bwd_same(const Problem& P, const float* grad_out, const int32_t* argmax, void* grad_Q,
-                        void* grad_D, cudaStream_t stream) {
+                        void* grad_D, cudaStream_t stream, const FusedCe* ce = nullptr) {
     if (P.dtype == kF32)
-        return run_bwd(P, grad_out, argmax, static_cast<float*>(grad_Q), static_cast<float*>(grad_D), stream);
+        return run_bwd(P, grad_out, argmax, static_cast<float*>(grad_Q), static_cast<float*>(grad_D), stream, ce);
     int dev = 0;
     lik_status st = check_device(&dev);
     if (st != LIK_OK) return st;
@@ -314,11 +328,50 @@ lik_status run_bwd_same(const Problem& P, const float* grad_out, const int32_t* 
     if ((st = check_aligned(grad_Q, 16, "grad_Q")) != LIK_OK) return st;
     if ((st = check_aligned(grad_D, 16, "grad_D")) != LIK_OK) return st;
     cudaError_t e;
-    if (grad_Q && (e = launch_bwd_grad_q_same(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess)
+    if (ce) {
+        e = launch_bwd_grad_q_ce(P, ce->scores, ce->target, ce->scale, ce->row_loss,
+                                 const_cast<float*>(grad_out), argmax, grad_Q, true, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "grad_Q launch (with the loss head)");
+    } else if (grad_Q && (e = launch_bwd_grad_q_same(P, grad_out, argmax, grad_Q, stream)) != cudaSuccess) {
         return cuda_fail(e, "grad_Q launch");
+    }
     if (grad_D && (e = launch_bwd_grad_d_same(P, grad_out, argmax, grad_D, stream)) != cudaSuccess)
         return cuda_fail(e, "grad_D launch");
     return LIK_OK;
+}
+
+// One loss-head step after the forward: with both gradients requested and the
+// shape in range, the loss head runs inside the backward's launches (the row
+// losses and the score gradient in the grad_Q gather, their mean in the grad_D
+// launch); otherwise lik_ce_rows and then the backward.
+lik_status ce_head_and_bwd(const Problem& P, const float* scores, const int32_t* target, float scale, float* loss,
+                           float* row_loss, float* grad_scores, const int32_t* argmax, void* grad_Q, void* grad_D,
+                           bool same_dtype, cudaStream_t stream, bool* fused) {
+    *fused = false;
+    if (!grad_Q || !grad_D || !grad_q_ce_fusable(P)) return LIK_OK;
+    int dev = 0;
+    lik_status st = check_device(&dev);
+    if (st != LIK_OK) return st;
+    const int64_t rows = P.n_query, cols = P.pairs_per_query;
+    const Spec specs[] = {
+        {"scores", scores, true, rows * cols},
+        {"target", target, true, rows},
+        {"loss", loss, true, 1},
+        {"row_loss", row_loss, true, rows},
+        {"grad_scores", grad_scores, true, rows * cols},
+    };
+    if ((st = check_buffers(dev, specs, 5)) != LIK_OK) return st;
+    if ((st = check_aligned(target, 4, "target")) != LIK_OK) return st;
+    if ((st = check_aligned(loss, 4, "loss")) != LIK_OK) return st;
+    if ((st = check_aligned(row_loss, 4, "row_loss")) != LIK_OK) return st;
+    if ((st = check_aligned(grad_scores, 4, "grad_scores")) != LIK_OK) return st;
+    const FusedCe ce{scores, target, scale, row_loss};
+    Problem Pc = P;  // the grad_D launch also writes the mean of the row losses
+    Pc.ce_loss = loss;
+    Pc.ce_row_loss = row_loss;
+    *fused = true;
+    if (same_dtype) return run_bwd_same(Pc, grad_scores, argmax, grad_Q, grad_D, stream, &ce);
+    return run_bwd(Pc, grad_scores, argmax, static_cast<float*>(grad_Q), static_cast<float*>(grad_D), stream, &ce);
 }
 
 }  // namespace
@@ -574,6 +627,13 @@ lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype d
     lik_status st = lik_maxsim_allpairs_fwd(Q, D, dtype, Nq, Nd, Lq, Ld, dim, qmask, dmask, scores, argmax, stream);
     if (st != LIK_OK) return st;
     if (Nq > 0 && Nd > 0 && !grad_scores) return fail(LIK_ERR_INVALID_ARG, "grad_scores is NULL");
+    if (Nq > 0 && Nd > 0) {
+        const Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+        bool fused = false;
+        st = ce_head_and_bwd(P, scores, target, scale, loss, row_loss, grad_scores, argmax, grad_Q, grad_D,
+                             grads_in_input_dtype != 0, stream, &fused);
+        if (st != LIK_OK || fused) return st;
+    }
     st = lik_ce_rows(scores, Nq, Nd, target, scale, loss, row_loss, grad_scores, stream);
     if (st != LIK_OK) return st;
     if (grads_in_input_dtype)
@@ -591,6 +651,13 @@ lik_status lik_maxsim_kd_ce_step(const void* Q, const void* D, lik_dtype dtype, 
     lik_status st = lik_maxsim_kd_fwd(Q, D, dtype, B, N, Lq, Ld, dim, qmask, dmask, scores, argmax, stream);
     if (st != LIK_OK) return st;
     if (B > 0 && N > 0 && !grad_scores) return fail(LIK_ERR_INVALID_ARG, "grad_scores is NULL");
+    if (B > 0 && N > 0) {
+        const Problem P = make_problem(kKd, dtype, Q, D, qmask, dmask, B, B * N, N, B * N, Lq, Ld, dim);
+        bool fused = false;
+        st = ce_head_and_bwd(P, scores, target, scale, loss, row_loss, grad_scores, argmax, grad_Q, grad_D,
+                             grads_in_input_dtype != 0, stream, &fused);
+        if (st != LIK_OK || fused) return st;
+    }
     st = lik_ce_rows(scores, B, N, target, scale, loss, row_loss, grad_scores, stream);
     if (st != LIK_OK) return st;
     if (grads_in_input_dtype)

@@ -88,18 +88,72 @@ __device__ __forceinline__ void store1(float* out, float v) { *out = v; }
 __device__ __forceinline__ void store1(__nv_bfloat16* out, float v) { *out = __float2bfloat16_rn(v); }
 __device__ __forceinline__ void store1(__half* out, float v) { *out = __float2half_rn(v); }
 
-// VECS vectors of 8 elements per thread: dim <= VECS * 64.
-template <typename T, int VECS, int kUnroll, typename TO>
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// The loss mean of a one-call loss-head step (Problem::ce_loss), written by
+// warp 0 of block 0 of the grad_D launch: lane l sums rows l, l + 32, ... in
+// order, then a fixed butterfly.
+__device__ __forceinline__ void ce_loss_mean(const Problem& P) {
+    if (P.ce_loss == nullptr || blockIdx.x != 0 || threadIdx.x >= 32) return;
+    float acc = 0.0f;
+    for (int64_t r = threadIdx.x; r < P.n_query; r += 32) acc += P.ce_row_loss[r];
+    acc = warp_sum_f(acc);
+    if (threadIdx.x == 0) *P.ce_loss = acc / static_cast<float>(P.n_query);
+}
+
+// Log-sum-exp of the logits scale * s[0, cols) (one warp; every lane gets it),
+// reduced in a fixed order.
+__device__ __forceinline__ float ce_row_lse(const float* s, int64_t cols, float scale, int lane) {
+    float m = -INFINITY;
+    for (int64_t c = lane; c < cols; c += 32) m = fmaxf(m, scale * s[c]);
+    m = warp_max_f(m);
+    float sum = 0.0f;
+    for (int64_t c = lane; c < cols; c += 32) sum += expf(scale * s[c] - m);
+    return m + logf(warp_sum_f(sum));
+}
+
+// Softmax cross-entropy over the score rows, computed by the grad_Q gather
+// (the loss head of lik_maxsim_*_ce_step): row r = query r, cols = its pairs.
+struct CeHead {
+    const float* scores;   // [rows, cols]
+    const int32_t* target; // [rows]; outside [0, cols): the row is left out
+    float scale;
+    float* row_loss;       // [rows]
+    float* grad;           // [rows, cols]: d loss / d scores, the backward's upstream gradient
+};
+
+// VECS vectors of 8 elements per thread: dim <= VECS * 64.  With kCE the
+// upstream gradient is not read but computed from the scores (CeHead): the
+// CTA's warp 0 takes its query row's log-sum-exp, the first CTA of each query
+// writes the row's loss and gradient (which grad_D then reads; the grad_D
+// launch also takes the mean of the row losses).
+template <typename T, int VECS, int kUnroll, typename TO, bool kCE = false>
 __global__ void __launch_bounds__(kVecThreads)
 grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
-                  TO* __restrict__ gQ, unsigned int* err) {
+                  TO* __restrict__ gQ, unsigned int* err, CeHead ce = CeHead()) {
     __shared__ int s_am[kPairChunk][kRowsPerCta];
     __shared__ float s_g[kPairChunk];
     __shared__ float s_part[kRowsPerCta][VECS * kThreadsPerRow * kVec];
+    __shared__ float s_lse;
+    __shared__ int s_t;
     const T* D = static_cast<const T*>(P.D);
     const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
     const int64_t q = blockIdx.x / groups;
     const int64_t i0 = (blockIdx.x - q * groups) * kRowsPerCta;
+    const int64_t cols = P.pairs_per_query;
+    const float inv_rows = 1.0f / static_cast<float>(P.n_query);
+    if constexpr (kCE) {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    }
     const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group
     const int tl = threadIdx.x % (kRowsPerCta * kThreadsPerRow);
     const int r = tl / kThreadsPerRow, sub = tl % kThreadsPerRow;
@@ -116,11 +170,41 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
     for (int64_t c0 = 0; c0 < P.pairs_per_query; c0 += kPairChunk) {
         const int nc = static_cast<int>(P.pairs_per_query - c0 < kPairChunk ? P.pairs_per_query - c0 : kPairChunk);
         __syncthreads();
-        for (int e = threadIdx.x; e < nc * kRowsPerCta; e += kVecThreads) {
-            const int t = e / kRowsPerCta, rr = e % kRowsPerCta;
-            s_am[t][rr] = rr < rows_here ? am[(p0 + c0 + t) * P.Lq + i0 + rr] : -1;
+        // with the loss head, warp 0 first takes the row's log-sum-exp while the
+        // other warps stage the first chunk's argmax
+        const int stage_lo = (kCE && c0 == 0) ? 32 : 0;
+        if (static_cast<int>(threadIdx.x) >= stage_lo) {
+            for (int e = threadIdx.x - stage_lo; e < nc * kRowsPerCta; e += kVecThreads - stage_lo) {
+                const int t = e / kRowsPerCta, rr = e % kRowsPerCta;
+                s_am[t][rr] = rr < rows_here ? am[(p0 + c0 + t) * P.Lq + i0 + rr] : -1;
+            }
+        } else if constexpr (kCE) {
+            const int lane = threadIdx.x & 31;
+            const int32_t t = ce.target[q];
+            const float* srow = ce.scores + q * cols;
+            const float lse = ce_row_lse(srow, cols, ce.scale, lane);
+            if (lane == 0) {
+                s_lse = lse;
+                s_t = t;
+                if (i0 == 0) ce.row_loss[q] = (t >= 0 && t < cols) ? lse - ce.scale * srow[t] : 0.0f;
+            }
         }
-        for (int t = threadIdx.x; t < nc; t += kVecThreads) s_g[t] = g[p0 + c0 + t];
+        if constexpr (kCE) {
+            if (c0 == 0) __syncthreads();  // s_lse, s_t
+            const float lse = s_lse;
+            const int32_t tq = s_t;
+            const bool row_in = tq >= 0 && tq < cols;
+            for (int t = threadIdx.x; t < nc; t += kVecThreads) {
+                const int64_t c = c0 + t;
+                const float gv = row_in ? ce.scale * (expf(ce.scale * ce.scores[q * cols + c] - lse) -
+                                                      (c == tq ? 1.0f : 0.0f)) * inv_rows
+                                        : 0.0f;
+                s_g[t] = gv;
+                if (i0 == 0) ce.grad[q * cols + c] = gv;
+            }
+        } else {
+            for (int t = threadIdx.x; t < nc; t += kVecThreads) s_g[t] = g[p0 + c0 + t];
+        }
         __syncthreads();
         if (r >= rows_here) continue;
         // this half takes pairs t = pg, pg + 2, pg + 4, ... of the chunk
@@ -258,6 +342,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 grad_d_scatter_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
                           float* __restrict__ gD, unsigned int* err) {
+    ce_loss_mean(P);
     const T* Q = static_cast<const T*>(P.Q);
     const int lane = threadIdx.x & 31;
     // one warp per pair; its query tokens' argmax are loaded 32 at a time
@@ -304,6 +389,7 @@ __global__ void __launch_bounds__(kThreads)
 grad_d_scatter_atomic_kernel(Problem P, const float* __restrict__ g,
                              const int32_t* __restrict__ am, float* __restrict__ gD,
                              unsigned int* err) {
+    ce_loss_mean(P);
     const T* Q = static_cast<const T*>(P.Q);
     const int lane = threadIdx.x & 31;
     const int64_t hits = P.n_pairs * P.Lq;
@@ -341,6 +427,7 @@ template <typename T, int VECS, typename TO>
 __global__ void __launch_bounds__(kThreads)
 grad_d_doc_stream_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
                          TO* __restrict__ gD, unsigned int* err) {
+    ce_loss_mean(P);
     __shared__ int s_row[32], s_qrow[32], s_nh;
     __shared__ float s_g;
     const T* Q = static_cast<const T*>(P.Q);
@@ -420,6 +507,7 @@ template <typename T, typename TO>
 __global__ void __launch_bounds__(kThreads)
 grad_d_chunk_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
                     TO* __restrict__ gD, int64_t rows_per_cta, int64_t chunks, unsigned int* err) {
+    ce_loss_mean(P);
     extern __shared__ float s_acc[];                              // rows x dim
     int* s_row = reinterpret_cast<int*>(s_acc + kChunkFloats);  // [kChunkRound]
     const T* Q = static_cast<const T*>(P.Q);
@@ -519,6 +607,7 @@ template <typename T, int VECS, typename TO>
 __global__ void __launch_bounds__(kThreads, 3)
 grad_d_owner_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
                     TO* __restrict__ gD, int64_t chunks, unsigned int* err) {
+    ce_loss_mean(P);
     __shared__ int2 s_hit[kOwnWindow];             // (Q row, pair) in bucket order
     __shared__ int s_cnt[kOwnRows * kWarps];       // per (row, warp), row-major; then offsets
     __shared__ int s_start[kOwnRows + 1];          // first hit of each row in s_hit
@@ -672,6 +761,20 @@ cudaError_t grad_q_typed(const Problem& P, const float* g, const int32_t* am, TO
     return cudaGetLastError();
 }
 
+template <typename T, typename TO>
+cudaError_t grad_q_ce_typed(const Problem& P, const CeHead& ce, const int32_t* am, TO* gQ, cudaStream_t stream,
+                            unsigned int* err) {
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t blocks = P.n_query * groups;
+    if (P.dim <= 128)
+        grad_q_vec_kernel<T, 2, 8, TO, true><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(
+            P, nullptr, am, gQ, err, ce);
+    else
+        grad_q_vec_kernel<T, 4, 4, TO, true><<<static_cast<unsigned>(blocks), kVecThreads, 0, stream>>>(
+            P, nullptr, am, gQ, err, ce);
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t grad_d_typed(const Problem& P, const float* g, const int32_t* am, float* gD,
                          cudaStream_t stream, unsigned int* err) {
@@ -763,6 +866,29 @@ cudaError_t launch_bwd_grad_q_same(const Problem& P, const float* g, const int32
     unsigned int* err = device_error_word();
     if (P.dtype == kF16) return grad_q_typed<__half, __half>(P, g, am, static_cast<__half*>(gQ), stream, err);
     return grad_q_typed<__nv_bfloat16, __nv_bfloat16>(P, g, am, static_cast<__nv_bfloat16*>(gQ), stream, err);
+}
+
+bool grad_q_ce_fusable(const Problem& P) {
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    return P.Lq >= 1 && P.n_query >= 1 && P.pairs_per_query >= 1 && P.dim % kVec == 0 && P.dim <= 256 &&
+           P.n_query * groups < (int64_t(1) << 31) && P.n_query * P.pairs_per_query <= (int64_t(1) << 20);
+}
+
+cudaError_t launch_bwd_grad_q_ce(const Problem& P, const float* scores, const int32_t* target, float scale,
+                                 float* row_loss, float* grad_scores, const int32_t* am, void* gQ, bool same_dtype,
+                                 cudaStream_t stream) {
+    unsigned int* err = device_error_word();
+    CeHead ce{scores, target, scale, row_loss, grad_scores};
+    if (!same_dtype || P.dtype == kF32) {
+        float* o = static_cast<float*>(gQ);
+        switch (P.dtype) {
+        case kF32: return grad_q_ce_typed<float, float>(P, ce, am, o, stream, err);
+        case kF16: return grad_q_ce_typed<__half, float>(P, ce, am, o, stream, err);
+        default: return grad_q_ce_typed<__nv_bfloat16, float>(P, ce, am, o, stream, err);
+        }
+    }
+    if (P.dtype == kF16) return grad_q_ce_typed<__half, __half>(P, ce, am, static_cast<__half*>(gQ), stream, err);
+    return grad_q_ce_typed<__nv_bfloat16, __nv_bfloat16>(P, ce, am, static_cast<__nv_bfloat16*>(gQ), stream, err);
 }
 
 cudaError_t launch_bwd_grad_d_same(const Problem& P, const float* g, const int32_t* am, void* gD,

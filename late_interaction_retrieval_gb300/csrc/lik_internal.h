@@ -34,6 +34,11 @@ struct Problem {
     int64_t pairs_per_query;  // Nd | 1 | N
     int64_t n_pairs;          // Nq*Nd | B | B*N
     int64_t Lq, Ld, dim;
+    // Set only for the backward of a one-call loss-head step: the grad_D launch
+    // also writes *ce_loss = the mean of ce_row_loss[0, n_query), summed in a
+    // fixed order (the row losses come from the grad_Q launch before it).
+    float* ce_loss = nullptr;
+    const float* ce_row_loss = nullptr;
 
     __host__ __device__ int64_t query_of(int64_t p) const { return p / pairs_per_query; }
     __host__ __device__ int64_t doc_of(int64_t p) const {
@@ -102,6 +107,16 @@ cudaError_t launch_bwd_grad_q_same(const Problem& P, const float* grad_out, cons
                                    void* grad_Q, cudaStream_t stream);
 cudaError_t launch_bwd_grad_d_same(const Problem& P, const float* grad_out, const int32_t* argmax,
                                    void* grad_D, cudaStream_t stream);
+
+// The grad_Q gather with the cross-entropy head over the score rows (row =
+// query, cols = its pairs) computed inside it: it writes the row losses and
+// the score gradient, which the grad_D launch then reads (with
+// Problem::ce_loss set, that launch also writes the losses' mean).  Needs
+// Lq >= 1, dim % 8 == 0, dim <= 256, rows * cols <= 2^20.
+bool grad_q_ce_fusable(const Problem& P);
+cudaError_t launch_bwd_grad_q_ce(const Problem& P, const float* scores, const int32_t* target, float scale,
+                                 float* row_loss, float* grad_scores, const int32_t* am, void* gQ, bool same_dtype,
+                                 cudaStream_t stream);
 
 // Softmax cross-entropy over score rows: per-row losses, their mean and the
 // gradient with respect to the scores (grad may be NULL).

@@ -97,3 +97,56 @@ def test_ce_step_matches_oracle(layout, nq, nd, lq, ld, dim, grads):
     tol = 2 * parity.TOL["bf16"] + extra
     assert parity.normwise_rel_err(gQ.float().cpu().numpy(), gQ_o) <= tol
     assert parity.normwise_rel_err(gD.float().cpu().numpy(), gD_o) <= tol
+
+
+@pytest.mark.parametrize("grads", ["f32", "input"])
+@pytest.mark.parametrize("layout,nq,nd,lq,ld,dim,dtype", [("allpairs", 6, 6, 32, 260, 128, "bf16"),
+                                                          ("kd", 4, 5, 32, 200, 128, "bf16"),
+                                                          ("allpairs", 5, 9, 20, 100, 64, "bf16"),
+                                                          ("allpairs", 4, 7, 16, 90, 64, "f32"),
+                                                          ("kd", 3, 6, 12, 70, 32, "f16")])
+def test_ce_step_head_inside_backward(layout, nq, nd, lq, ld, dim, dtype, grads):
+    """With both gradients requested, the one-call step computes the loss head
+    inside the backward's launches (row losses and score gradient in the grad_Q
+    gather, their mean in the grad_D launch).  Its loss, row losses and score
+    gradient must agree with the separate head (lik_ce_rows) on the step's own
+    scores, the loss must be bit-identical from call to call (fixed summation
+    order), and the steps without grad_Q or without grad_D (separate head) must
+    give the same loss and gradients."""
+    inp = separated_case(layout, nq, nd, lq, ld, dim, dtype, seed=nq * 13 + nd, p_doc_empty=0.0)
+    h = gpu_harness.Layout(inp)
+    rows, cols = nq, nd
+    target = np.arange(rows, dtype=np.int32) % cols if layout == "allpairs" else np.zeros(rows, np.int32)
+    target[0] = cols + 1  # a row left out of the loss
+    Q, D, qm, dm = h.gpu_inputs()
+    dev = "cuda"
+    gdt = Q.dtype if grads == "input" else torch.float32
+    tt = torch.as_tensor(target, device=dev)
+    step = getattr(binding, f"lik_maxsim_{layout}_ce_step")
+
+    def run(with_q=True, with_d=True):
+        out = dict(scores=torch.empty(rows, cols, device=dev), am=torch.empty(rows, cols, lq, dtype=torch.int32, device=dev),
+                   loss=torch.empty(1, device=dev), rl=torch.empty(rows, device=dev), gs=torch.empty(rows, cols, device=dev),
+                   gQ=torch.empty(Q.shape, dtype=gdt, device=dev) if with_q else None,
+                   gD=torch.empty(D.shape, dtype=gdt, device=dev) if with_d else None)
+        step(Q, D, qm, dm, tt, out["scores"], out["am"], out["loss"], out["rl"], out["gs"], out["gQ"], out["gD"],
+             scale=1.3)
+        binding.lik_check_device_error()
+        return out
+
+    a, b, c, d = run(), run(), run(with_q=False), run(with_d=False)
+    assert a["loss"].item() == b["loss"].item()
+    loss = torch.empty(1, device=dev)
+    rl = torch.empty(rows, device=dev)
+    gs = torch.empty(rows, cols, device=dev)
+    binding.lik_ce_rows(a["scores"], tt, loss, rl, gs, scale=1.3)
+    torch.cuda.synchronize()
+    assert abs(a["loss"].item() - loss.item()) <= 1e-6 * max(1.0, abs(loss.item()))
+    assert parity.normwise_rel_err(a["rl"].cpu().numpy(), rl.cpu().numpy()) <= 1e-6
+    assert parity.normwise_rel_err(a["gs"].cpu().numpy(), gs.cpu().numpy()) <= 1e-6
+    assert float(a["rl"][0]) == 0.0 and torch.all(a["gs"][0] == 0)
+    # the separate-head paths (no grad_Q, or no grad_D) give the same loss and gradients
+    assert parity.normwise_rel_err(c["gD"].float().cpu().numpy(), a["gD"].float().cpu().numpy()) <= 1e-5
+    assert parity.normwise_rel_err(d["gQ"].float().cpu().numpy(), a["gQ"].float().cpu().numpy()) <= 1e-5
+    for other in (c, d):
+        assert abs(other["loss"].item() - a["loss"].item()) <= 1e-6 * max(1.0, abs(a["loss"].item()))
