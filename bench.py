@@ -1,11 +1,14 @@
 """Benchmark of the MaxSim hot path on GB300.
 
-Default workload: the in-batch contrastive all-pairs forward + backward, bf16
-in / fp32 scores, Q[128,32,128] x D[128,1030,128], document lengths
-U[700,1030], grad_out from row-wise cross-entropy with the diagonal as
-target.  One step = liblik forward (scores + saved argmax) and backward
-(grad_Q, grad_D) through the C ABI, inputs resident in HBM.  The headline
-metric counts 2*Nq*Nd*Lq*Ld*dim FLOPs (padded Ld) per step.
+Default workload: the in-batch contrastive all-pairs training step, bf16 in /
+fp32 scores, Q[128,32,128] x D[128,1030,128], document lengths U[700,1030],
+the loss the cross-entropy over the score rows with the diagonal as target.
+One step = one liblik call (lik_maxsim_allpairs_ce_step: forward with the
+saved argmax, the loss and its score gradient, backward to fp32 grad_Q and
+grad_D) through the C ABI, inputs resident in HBM; --step fwd+bwd times the
+forward and backward calls with the score gradient computed once outside the
+steps instead.  The headline metric counts 2*Nq*Nd*Lq*Ld*dim FLOPs (padded Ld)
+per step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, as it stands
@@ -453,10 +456,16 @@ def backward_roofline(st: Step, args, stream, flush, peaks) -> dict:
     return {"grad_q": gq, "grad_d": gd}
 
 
+def has_ce_head(name: str) -> bool:
+    """The workload's upstream gradient comes from a cross-entropy over its score rows."""
+    return name in ("inbatch_b128_bf16", "inbatch_b128_f32", "kd_b256_n17_bf16")
+
+
 def config_record(name: str, device, args, stream, flush, peaks) -> dict:
     """One extra workload measured like the headline one (same steps, L2
-    flush and clock sampling), as a record of the line's "configs"."""
-    st = Step(name, device, "f32")
+    flush and clock sampling; its training step in one call when it has a
+    cross-entropy head), as a record of the line's "configs"."""
+    st = Step(name, device, "f32", ce=has_ce_head(name))
     w = st.w
     t = timed_steps(st, args, stream, flush, 1)
     ms = statistics.mean(t["step_ms"])
@@ -473,6 +482,7 @@ def config_record(name: str, device, args, stream, flush, peaks) -> dict:
            "gpu_launches": st.launches_per_step * args.steps}
     if w.backward:
         rec["grad_dtype"] = "f32"
+        rec["loss_head"] = "cross-entropy inside the step (one call)" if st.ce else "score gradient precomputed"
         rec["roofline_bwd"] = backward_roofline(st, args, stream, flush, peaks)
     del st
     torch.cuda.empty_cache()
@@ -528,7 +538,7 @@ def run_ours(args):
 
     # ---- the other workloads, one record each (single GPU, default step only)
     configs = None
-    if world == 1 and not args.no_extra_configs and args.step == "fwd+bwd" and args.grad_dtype == "f32":
+    if world == 1 and not args.no_extra_configs and args.step in ("fwd+bwd", "ce") and args.grad_dtype == "f32":
         del st
         torch.cuda.empty_cache()
         configs = {n: config_record(n, device, args, stream, flush, peaks) for n in EXTRA_WORKLOADS if n != name}
@@ -732,14 +742,18 @@ def main():
     ap.add_argument("--no-extra-configs", action="store_true",
                     help="measure only --workload (by default a single-GPU run of the default step also "
                          "measures the per-query-candidate, reranking and large all-pairs workloads)")
-    ap.add_argument("--step", choices=["fwd+bwd", "ce", "recompute"], default="fwd+bwd",
-                    help="ce: the workload's cross-entropy head (loss and score gradient) inside every step; "
-                         "recompute: the forward saves no argmax and the backward recomputes it")
+    ap.add_argument("--step", choices=["auto", "fwd+bwd", "ce", "recompute"], default="auto",
+                    help="ce: the workload's training step in one call (forward, cross-entropy head, backward); "
+                         "fwd+bwd: forward and backward with the score gradient computed once outside the steps; "
+                         "recompute: the forward saves no argmax and the backward recomputes it; "
+                         "auto (default): ce for workloads with a cross-entropy head, else fwd+bwd")
     ap.add_argument("--grad-dtype", choices=["f32", "input"], default="f32",
                     help="gradients in fp32 (default) or in the inputs' dtype (the _bwd_same_dtype entry points)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.step == "auto":
+        args.step = "ce" if has_ce_head(args.workload) else "fwd+bwd"
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -340,6 +340,27 @@ lik_status run_bwd_same(const Problem& P, const float* grad_out, const int32_t* 
     return LIK_OK;
 }
 
+// In a one-call step whose backward writes an fp32 grad_D on the same stream
+// right after the forward, the tensor-core all-pairs forward zero-fills that
+// grad_D on the side (HBM is mostly idle while it runs), and the backward
+// skips its own zero-fill.  Only for a grad_D that the backward will accept
+// (device memory of the current device, 16-byte aligned); otherwise nothing
+// changes and the backward reports what is wrong.
+void plan_fwd_zero(Problem& P, float* grad_D) {
+    if (!grad_D || P.layout != kAllPairs || P.n_pairs * P.Lq == 0 || !tc_allpairs_eligible(P)) return;
+    const int64_t elems = P.n_doc * P.Ld * P.dim;
+    if (elems % 4 != 0 || (reinterpret_cast<uintptr_t>(grad_D) & 15) != 0) return;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return;
+    if (check_pointer(grad_D, dev, "grad_D") != LIK_OK) {
+        t_message[0] = 0;
+        return;
+    }
+    P.fwd_zero = grad_D;
+    P.fwd_zero_bytes = elems * static_cast<int64_t>(sizeof(float));
+    P.grad_d_zeroed = true;
+}
+
 // One loss-head step after the forward: with both gradients requested and the
 // shape in range, the loss head runs inside the backward's launches (the row
 // losses and the score gradient in the grad_Q gather, their mean in the grad_D
@@ -624,11 +645,17 @@ lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype d
                                        int32_t* argmax, float* loss, float* row_loss, float* grad_scores,
                                        void* grad_Q, void* grad_D, int grads_in_input_dtype,
                                        cudaStream_t stream) {
-    lik_status st = lik_maxsim_allpairs_fwd(Q, D, dtype, Nq, Nd, Lq, Ld, dim, qmask, dmask, scores, argmax, stream);
+    t_message[0] = 0;
+    bool nothing = false;
+    lik_status st = check_common(dtype, Nq, Nd, Nd, Lq, Ld, dim, &nothing);
     if (st != LIK_OK) return st;
+    Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
+    if (!nothing) {
+        if (!grads_in_input_dtype || dtype == LIK_F32) plan_fwd_zero(P, static_cast<float*>(grad_D));
+        if ((st = run_fwd(P, qmask, dmask, scores, argmax, stream)) != LIK_OK) return st;
+    }
     if (Nq > 0 && Nd > 0 && !grad_scores) return fail(LIK_ERR_INVALID_ARG, "grad_scores is NULL");
     if (Nq > 0 && Nd > 0) {
-        const Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
         bool fused = false;
         st = ce_head_and_bwd(P, scores, target, scale, loss, row_loss, grad_scores, argmax, grad_Q, grad_D,
                              grads_in_input_dtype != 0, stream, &fused);
@@ -678,7 +705,10 @@ lik_status lik_maxsim_allpairs_bwd_recompute(const void* Q, const void* D, lik_d
     if (st != LIK_OK) return st;
     Problem P = make_problem(kAllPairs, dtype, Q, D, qmask, dmask, Nq, Nd, Nd, Nq * Nd, Lq, Ld, dim);
     if (nothing) P.n_pairs = 0;
-    if (!nothing && (st = run_fwd(P, qmask, dmask, nullptr, argmax_workspace, stream, true)) != LIK_OK) return st;
+    if (!nothing) {
+        plan_fwd_zero(P, grad_D);
+        if ((st = run_fwd(P, qmask, dmask, nullptr, argmax_workspace, stream, true)) != LIK_OK) return st;
+    }
     return run_bwd(P, grad_out, argmax_workspace, grad_Q, grad_D, stream);
 }
 

@@ -151,9 +151,6 @@ grad_q_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restr
     const int64_t i0 = (blockIdx.x - q * groups) * kRowsPerCta;
     const int64_t cols = P.pairs_per_query;
     const float inv_rows = 1.0f / static_cast<float>(P.n_query);
-    if constexpr (kCE) {
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    }
     const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group
     const int tl = threadIdx.x % (kRowsPerCta * kThreadsPerRow);
     const int r = tl / kThreadsPerRow, sub = tl % kThreadsPerRow;
@@ -803,8 +800,10 @@ cudaError_t launch_bwd_grad_d(const Problem& P, const float* g, const int32_t* a
                               cudaStream_t stream) {
     const int64_t elems = P.n_doc * P.Ld * P.dim;
     if (elems == 0) return cudaSuccess;
-    const cudaError_t e = cudaMemsetAsync(gD, 0, sizeof(float) * elems, stream);
-    if (e != cudaSuccess) return e;
+    if (!P.grad_d_zeroed) {  // else the forward of the same step has zero-filled it
+        const cudaError_t e = cudaMemsetAsync(gD, 0, sizeof(float) * elems, stream);
+        if (e != cudaSuccess) return e;
+    }
     if (P.n_pairs * P.Lq == 0) return cudaSuccess;
     unsigned int* err = device_error_word();
     switch (P.dtype) {

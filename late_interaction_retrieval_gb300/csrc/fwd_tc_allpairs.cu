@@ -33,6 +33,10 @@
 //               epilogue and the MMA continue.
 //   warp 19     MMA issuer of the odd tiles (one issuing thread leaves the
 //               tensor pipe idle while it checks barriers between chains)
+// Lanes 1-31 of the producer warp zero-fill a buffer of the backward that
+// follows on the stream, when there is one (the fp32 grad_D of a one-call
+// training step), while the tensor cores keep the kernel busy and HBM is
+// mostly idle.
 // The accumulator is multi-buffered in TMEM (512 columns split into 2..4
 // buffers, as many as the tile width allows), so the MMA runs ahead of the
 // epilogue.
@@ -88,6 +92,8 @@ struct Params {
     float* scores;
     int32_t* argmax;
     unsigned int* err;
+    float4* zero;           // a buffer the kernel zero-fills on the side (nullptr: none)
+    int64_t zero_n16;       // its size in 16-byte words
 };
 
 // Barrier slots in the misc region.
@@ -260,7 +266,14 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
 
     if (warp == 0) {
         // ------------------------------------------------------ producer --
-        if (lane == 0) {
+        if (lane != 0) {
+            // the side zero-fill: 16-byte stores, 31 lanes of every CTA over
+            // the buffer, each warp instruction 496 contiguous bytes
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int64_t i = static_cast<int64_t>(blockIdx.x) * 31 + lane - 1; i < p.zero_n16;
+                 i += static_cast<int64_t>(gridDim.x) * 31)
+                p.zero[i] = z;
+        } else {
             ptx::prefetch_tmap(&tmq);
             ptx::prefetch_tmap(&tmd);
             int s = 0, qb = 0;
@@ -675,6 +688,8 @@ cudaError_t launch_fwd_tc_allpairs(const Problem& P, float* scores, int32_t* arg
     p.scores = scores;
     p.argmax = argmax;
     p.err = device_error_word();
+    p.zero = static_cast<float4*>(P.fwd_zero);
+    p.zero_n16 = P.fwd_zero ? P.fwd_zero_bytes / 16 : 0;
 
     CUtensorMap tmq, tmd;
     {

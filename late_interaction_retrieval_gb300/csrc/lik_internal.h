@@ -39,6 +39,13 @@ struct Problem {
     // fixed order (the row losses come from the grad_Q launch before it).
     float* ce_loss = nullptr;
     const float* ce_row_loss = nullptr;
+    // Set only inside a one-call step whose backward follows on the stream:
+    // the tensor-core all-pairs forward zero-fills fwd_zero (fwd_zero_bytes, a
+    // multiple of 16, 16-byte aligned) on the side, and the fp32 grad_D launch
+    // of that backward then skips its own zero-fill (grad_d_zeroed).
+    void* fwd_zero = nullptr;
+    int64_t fwd_zero_bytes = 0;
+    bool grad_d_zeroed = false;
 
     __host__ __device__ int64_t query_of(int64_t p) const { return p / pairs_per_query; }
     __host__ __device__ int64_t doc_of(int64_t p) const {
