@@ -513,9 +513,9 @@ def run_ours(args):
     # ---- end to end through the public API: pinned host inputs in, results out
     e2e = run_e2e(st, args, stream, world)
 
-    # ---- each backward kernel on its own (plain fwd+bwd steps)
+    # ---- each backward kernel on its own (the plain backward entry point)
     bwd_roof = None
-    if w.backward and not st.ce and not st.recompute:
+    if w.backward and not st.recompute:
         bwd_roof = backward_roofline(st, args, stream, flush, peaks)
 
     fwd_bytes_step = st.algorithmic_bytes()

@@ -373,6 +373,15 @@ lik_status lik_ce_rows(const float* scores, int64_t rows, int64_t cols, const in
  * the _bwd_same_dtype entry points.  Arguments, shapes and errors as in the
  * entry points it calls; scores, argmax, loss, row_loss and grad_scores are
  * caller-allocated outputs.  It returns the first non-OK status.
+ *
+ * The results are those of the three calls in that order; the launches
+ * differ.  When grad_Q and grad_D are both given, dim % 8 == 0, dim <= 256
+ * and rows * cols <= 2^20, the loss head runs inside the backward: the
+ * grad_Q kernel computes each row's log-sum-exp, row_loss and grad_scores
+ * before it uses them, and the grad_D kernel's first block writes *loss (the
+ * same fixed-order mean).  With fp32 gradients and the fp16/bf16 all-pairs
+ * forward, the forward also zero-fills grad_D (16-byte aligned, element
+ * count a multiple of 4) on its producer warp instead of a separate memset.
  */
 lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
                                        int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,

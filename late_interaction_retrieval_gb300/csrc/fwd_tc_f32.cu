@@ -4,9 +4,10 @@
 // and "Scoring interface"): for every pair p of query q and document d of the
 // layout, score[p] = sum over valid i of max over valid j of Q[q,i].D[d,j],
 // the lowest j reaching each max saved as argmax, -1e9 for a document with no
-// valid token.  fp32 inputs keep fp32 accuracy (README, "Precision and
-// compatibility": fp32 inputs are accepted; their scores are held to 1e-5 of
-// an exact reference, which rules out rounding them to 16 bits).
+// valid token.  The README ("Precision and compatibility") accepts fp32
+// inputs; its own accelerated path rounds them to half precision.  Here fp32
+// inputs keep fp32 accuracy (scores within 1e-5 of an exact result), which
+// rules out rounding them to 16 bits.
 //
 // Split precision.  Every fp32 element x is split into two TF32 values
 // hi = round(x) and lo = round(x - hi) (round to nearest, 11 significant bits
