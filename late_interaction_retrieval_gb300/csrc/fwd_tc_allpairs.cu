@@ -66,7 +66,7 @@ namespace {
 
 constexpr int kEpiWarps = 16;         // 4 warpgroups of 4 warps
 constexpr int kEpiGroups = kEpiWarps / 4;
-constexpr int kRedWarps = 1;          // document-end reducer
+constexpr int kRedWarps = 1;          // document-end reducer (one warp: it synchronises with __syncwarp)
 constexpr int kIssuers = 2;           // MMA issuing threads (warp 1 and the last warp)
 constexpr int kThreads = 32 * (2 + kEpiWarps + kRedWarps + 1);
 constexpr int kSlots = 1;             // documents in flight between the epilogue and the reducers
@@ -101,10 +101,10 @@ struct Bars {
     uint64_t full_d[kMaxStages], empty_d[kMaxStages];
     uint64_t full_q[2], empty_q[2];
     uint64_t acc_full[kMaxAcc], acc_empty[kMaxAcc];
-    uint64_t xfull[kSlots];   // every epilogue thread has published a document's (max, argmax)
-    uint64_t xfree[kSlots];   // the reducers have read them
-    uint64_t rsum[kSlots];    // the reducers' per-row terms are in shared memory
+    uint64_t xfull[kSlots];   // every epilogue warp has published a document's (max, argmax)
+    uint64_t xfree[kSlots];   // the reducer has read them
     uint64_t mma_done;
+    uint64_t exit_bar;   // every warp is done (one arrive per warp): TMEM may be released
     uint32_t tmem_base;
     uint32_t pad;
 };
@@ -246,11 +246,13 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), kEpiWarps);
         }
         for (int b = 0; b < kSlots; ++b) {
-            ptx::mbar_init(ptx::smem_u32(&bars->xfull[b]), kEpiWarps * 32);
-            ptx::mbar_init(ptx::smem_u32(&bars->xfree[b]), kRedWarps * 32);
-            ptx::mbar_init(ptx::smem_u32(&bars->rsum[b]), kRedWarps * 32);
+            // one arrival per warp, after __syncwarp: a barrier word takes its
+            // arrivals one at a time, and a document end is on the epilogue's path
+            ptx::mbar_init(ptx::smem_u32(&bars->xfull[b]), kEpiWarps);
+            ptx::mbar_init(ptx::smem_u32(&bars->xfree[b]), 1);
         }
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), kIssuers);
+        ptx::mbar_init(ptx::smem_u32(&bars->exit_bar), kThreads / 32);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -430,7 +432,9 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
 #pragma unroll
             for (int k = 0; k < kUnitsPerGroup / 2; ++k) any = any || (mw[k] != 0);
 
-            ok = ptx::mbar_wait(ptx::smem_u32(&bars->acc_full[ab]), aph, err);
+            // the 16 epilogue warps poll with naps: the MMA issuers, the producer
+            // and the reducer share their SM sub-partitions
+            ok = ptx::mbar_wait_nap(ptx::smem_u32(&bars->acc_full[ab]), aph, err, 32);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -470,13 +474,14 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 if constexpr (kArg) {
                     if (bcol >= 0) am = bcol + first_equal16(best, m);
                 }
-                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfree[slot]), xph ^ 1, err);
+                ok = ptx::mbar_wait_nap(ptx::smem_u32(&bars->xfree[slot]), xph ^ 1, err, 32);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 xc->m[slot][wg][r] = m;
                 xc->a[slot][wg][r] = am;
                 if (lane == 0) xc->any[slot][wg][quarter] = any ? 1u : 0u;
-                ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[slot]));
+                __syncwarp();  // the warp's writes precede lane 0's arrive (release)
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[slot]));
                 if (++slot == kSlots) { slot = 0; xph ^= 1; }
             }
             cur = nxt;
@@ -489,6 +494,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         // greater wins, equal maxima keep the lower column), sum the valid
         // query tokens' maxima per query in a fixed order, write score and
         // argmax.  A thread owns rows rr + 32 * kRedWarps * k.
+        static_assert(kRedWarps == 1, "the reducer synchronises its lanes with __syncwarp");
         constexpr int kRows = kM / (32 * kRedWarps);
         const int rr = (warp - 2 - kEpiWarps) * 32 + lane;  // the reducer warp(s) follow the epilogue
         const int64_t qrows = static_cast<int64_t>(p.qpt) * Lq;
@@ -532,7 +538,9 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 qvalid[k] = qv_cur[k] != 0;
             }
             for (int64_t d = d0; ok && d < d1; ++d) {
-                ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull[slot]), xph, err);
+                // a document takes several tiles: nap between polls, the reducer
+                // shares its sub-partition with four epilogue warps
+                ok = ptx::mbar_wait_nap(ptx::smem_u32(&bars->xfull[slot]), xph, err, 128);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 int am[kRows];
@@ -557,11 +565,10 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                     xc->term[slot][r] = (an && qvalid[k]) ? mm : 0.0f;
                     am[k] = (an && qvalid[k]) ? aa : -1;
                 }
-                ptx::mbar_arrive(ptx::smem_u32(&bars->xfree[slot]));
-                ptx::mbar_arrive(ptx::smem_u32(&bars->rsum[slot]));
-                ok = ptx::mbar_wait(ptx::smem_u32(&bars->rsum[slot]), xph, err);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
+                // the warp's reads of the slot and its term writes are complete:
+                // release the slot, and make the terms visible to the summing lanes
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xfree[slot]));
 #pragma unroll
                 for (int k = 0; k < kRows; ++k) {
                     if (!row_ok[k]) continue;
@@ -590,9 +597,25 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         }
     }
 
+    // Release TMEM once every warp has finished with it: each warp arrives
+    // once on an mbarrier after its last tensor-memory access, and the
+    // allocating warp waits for all of them (bounded) before freeing the
+    // columns.  In the producer and the two MMA issuers, lane 0 alone did the work:
+    // it arrives for its warp and the other lanes leave (the allocating
+    // warp's lanes wait for lane 0 first, since the free is warp-wide).  An
+    // mbarrier rather than a CTA barrier: the warps arrive microseconds
+    // apart, and timing of this kernel showed bar.sync letting warps through
+    // before the last warp had arrived.
     ptx::tc_fence_before();
-    __syncthreads();
+    if (warp <= 1 || warp == 3 + kEpiWarps) {
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    } else {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    }
     if (warp == 1) {
+        __syncwarp();
+        ptx::mbar_wait(ptx::smem_u32(&bars->exit_bar), 0, p.err);
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }

@@ -95,6 +95,7 @@ struct Bars {
     uint64_t acc_full[kAcc], acc_empty[kAcc];
     uint64_t xfull[2];   // every epilogue thread has written a document's per-row terms
     uint64_t mma_done;
+    uint64_t exit_bar;   // every warp is done (one arrive per warp): TMEM may be released
     uint32_t tmem_base;
     uint32_t pad;
 };
@@ -220,8 +221,10 @@ allpairs_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmd, const Params p
             ptx::mbar_init(ptx::smem_u32(&bars->acc_full[b]), 1);
             ptx::mbar_init(ptx::smem_u32(&bars->acc_empty[b]), kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) ptx::mbar_init(ptx::smem_u32(&bars->xfull[b]), 32 * kEpiWarps);
+        // one arrival per epilogue warp (lane 0, after __syncwarp)
+        for (int b = 0; b < 2; ++b) ptx::mbar_init(ptx::smem_u32(&bars->xfull[b]), kEpiWarps);
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), kIssuers);
+        ptx::mbar_init(ptx::smem_u32(&bars->exit_bar), kThreads / 32);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -419,7 +422,8 @@ allpairs_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmd, const Params p
                 xc->term[xb][r] = live ? m : 0.0f;
                 // all rows written (bounded wait); the buffer is written again two
                 // documents later, after every thread has passed the next one's wait
-                ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[xb]));
+                __syncwarp();  // the warp's term writes precede lane 0's arrive (release)
+                if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[xb]));
                 ok = ptx::mbar_wait(ptx::smem_u32(&bars->xfull[xb]), (xph >> xb) & 1u, err);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
@@ -444,9 +448,25 @@ allpairs_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmd, const Params p
         }
     }
 
+    // Release TMEM once every warp has finished with it: each warp arrives
+    // once on an mbarrier after its last tensor-memory access, and the
+    // allocating warp waits for all of them (bounded) before freeing the
+    // columns.  In the producer and the two MMA issuers, lane 0 alone did the work:
+    // it arrives for its warp and the other lanes leave (the allocating
+    // warp's lanes wait for lane 0 first, since the free is warp-wide).  An
+    // mbarrier rather than a CTA barrier: the warps arrive microseconds
+    // apart, and timing of this kernel showed bar.sync letting warps through
+    // before the last warp had arrived.
     ptx::tc_fence_before();
-    __syncthreads();
+    if (warp <= 1 || warp == 2 + kConvWarps + kEpiWarps) {
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    } else {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    }
     if (warp == 1) {
+        __syncwarp();
+        ptx::mbar_wait(ptx::smem_u32(&bars->exit_bar), 0, p.err);
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, kTmemCols);
     }

@@ -137,8 +137,9 @@ struct Bars {
     uint64_t rec_full[kRing], rec_empty[kRing];
     uint64_t dump_full[2], dump_empty[2];  // update warps -> reducer warp
     uint64_t mma_done;
+    uint64_t exit_bar;   // every warp is done (one arrive per warp): TMEM may be released
     uint32_t tmem_base;
-    uint32_t pad;
+    uint32_t pad[3];     // Shared follows at a 16-byte boundary
 };
 
 // Per-document state handed from the update warps to the reducer warp
@@ -463,6 +464,7 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             ptx::mbar_init(ptx::smem_u32(&bars->rec_empty[r]), 4);
         }
         ptx::mbar_init(ptx::smem_u32(&bars->mma_done), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars->exit_bar), kThreads / 32);
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -872,9 +874,25 @@ stream_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         }
     }
 
+    // Release TMEM once every warp has finished with it: each warp arrives
+    // once on an mbarrier after its last tensor-memory access, and the
+    // allocating warp waits for all of them (bounded) before freeing the
+    // columns.  In the MMA issuer, lane 0 alone did the work:
+    // it arrives for its warp and the other lanes leave (the allocating
+    // warp's lanes wait for lane 0 first, since the free is warp-wide).  An
+    // mbarrier rather than a CTA barrier: the warps arrive microseconds
+    // apart, and timing of this kernel showed bar.sync letting warps through
+    // before the last warp had arrived.
     ptx::tc_fence_before();
-    __syncthreads();
     if (warp == 1) {
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    } else {
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->exit_bar));
+    }
+    if (warp == 1) {
+        __syncwarp();
+        ptx::mbar_wait(ptx::smem_u32(&bars->exit_bar), 0, p.err);
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, p.acc_cols);
     }

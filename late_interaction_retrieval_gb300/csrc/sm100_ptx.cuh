@@ -84,6 +84,36 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
     return mbar_wait_for(bar, parity, err, kWaitTimeoutNs);
 }
 
+// Non-blocking test of a phase (no suspend).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// mbar_wait for warps that share their SM sub-partition with busy warps:
+// between tests the waiting warp sleeps `nap_ns` (__nanosleep), so its polls
+// do not take issue slots from them.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_nap(uint32_t bar, uint32_t parity, unsigned int* err, unsigned nap_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+#pragma unroll 1
+    while (true) {
+        __nanosleep(nap_ns);
+        if (mbar_test_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA --
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
