@@ -26,7 +26,7 @@
 //               warpgroups split each tile's 16-column units round-robin
 //               (unit u goes to group u % 4) and keep a running (max, argmax)
 //               per row; at the end of a document each group hands its
-//               values to the reducers through shared memory
+//               values to the reducer through shared memory
 //               and goes on with the next document.
 //   warp 18     reducer: merges the four groups' values per row, sums each
 //               query's valid rows and writes the score and argmax, while the
@@ -49,8 +49,14 @@
 // When argmax is wanted, a unit whose max is strictly larger than the row's
 // running max keeps its 16 values in registers; at the document's end the
 // lowest column equal to the max is picked from them.  Exact ties therefore
-// go to the lowest token index, as in the oracle.  The reducers sum the
+// go to the lowest token index, as in the oracle.  The reducer sums the
 // maxima of the valid query tokens per query in a fixed order.
+//
+// Synchronisation: every hand-off is an mbarrier.  The epilogue warps and the
+// reducer count one arrival per warp (after __syncwarp) and poll their waits
+// with short naps, so that they take no issue slots from the MMA issuers,
+// the producer and the reducer that share their sub-partitions.  TMEM is
+// freed after an exit mbarrier that every warp arrives at once.
 //
 // Every mbarrier wait is bounded (ptx::mbar_wait); on expiry the kernel sets
 // the library's error word, drains its own TMA loads and MMAs, frees TMEM and
