@@ -665,6 +665,17 @@ def run_e2e(st: Step, args, stream, world):
     e1.record(s_out)  # after the last step's result copies (which follow all its work)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), st.device)
+    # the pipelined steps computed what a plain step computes: the last step's
+    # loss (or scores), copied to the host, equals a plain step's bit for bit
+    # (both are summed in a fixed order; the inputs are the same)
+    last = back[(k_next[0] - 1) % 2][0]
+    if st.ce:
+        st.ce_step()
+    else:
+        st.fwd()
+    plain = outs_of(st)[0].cpu()
+    if not torch.equal(last, plain):
+        raise RuntimeError("end-to-end pipeline: the last step's result differs from a plain step's")
     if w.layout == "pairwise" and not w.backward:
         val, unit = whole_job_rate(world, n, st.algorithmic_bytes(), ms, 1e9), "GB/s"
     else:
