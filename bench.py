@@ -13,8 +13,9 @@ per step.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 CPU oracle, as it stands
 
-The line also carries "roofline_bwd" (each backward kernel timed on its own,
-with the bytes it must move) and, in a single-GPU run of the default step,
+The line also carries "roofline_bwd" (the backward timed through its plain
+entry point, both gradients in the one launch the step runs and each gradient
+alone, with the bytes each must move) and, in a single-GPU run of the default step,
 "configs": one record per other workload (per-query candidates fwd+bwd,
 long-document reranking fwd, large all-pairs inference fwd, and the in-batch
 workload with fp32 inputs fwd+bwd), each measured
@@ -240,7 +241,7 @@ class Step:
 
     def ce_step(self, Q=None, D=None, qm=None, dm=None, target=None):
         """The workload's loss head in one call: forward, loss, backward (the
-        loss head runs inside the backward's first launch)."""
+        loss head runs inside the backward launch)."""
         i = self.inp
         getattr(self.binding, f"lik_maxsim_{self.layout}_ce_step")(
             i.Q if Q is None else Q, i.D if D is None else D, i.qmask if qm is None else qm,
@@ -261,14 +262,26 @@ class Step:
             i.Q if Q is None else Q, i.D if D is None else D, self.g if g is None else g,
             self.argmax, self.gQ, self.gD)
 
+    @property
+    def fused_bwd(self) -> bool:
+        """Whether the backward is one launch for both gradients: fp32
+        gradients, dim % 8 == 0, dim <= 256 and, with the loss head inside,
+        at most 4096 score rows (else one launch for each gradient)."""
+        w = self.w
+        rows = w.nq
+        cols = self.scores.numel() // rows
+        return (not self.same_dtype and w.dim % 8 == 0 and w.dim <= 256
+                and (not self.ce or (rows <= 4096 and rows * cols <= 1 << 20)))
+
     # launches of liblik kernels per step (cudaMemsetAsync of grad_D is not ours;
     # the streaming forward of the pairwise and kd layouts is a plan kernel and
     # the forward kernel; the cross-entropy head runs inside the backward's
-    # grad_Q launch; the recompute backward adds one forward)
+    # launch; the recompute backward adds one forward)
     @property
     def launches_per_step(self) -> int:
         fwd = 1 if self.layout == "allpairs" else 2
-        return fwd + (2 if self.w.backward else 0) + (fwd if self.recompute else 0)
+        bwd = (1 if self.fused_bwd else 2) if self.w.backward else 0
+        return fwd + bwd + (fwd if self.recompute else 0)
 
     def valid_flops(self) -> int:
         i, w = self.inp, self.w
@@ -397,8 +410,10 @@ def forward_roofline(st: Step, name: str, fwd_avg_ms: float, peaks) -> dict:
 
 
 def backward_roofline(st: Step, args, stream, flush, peaks) -> dict:
-    """Each backward kernel timed on its own (the entry point called with only
-    grad_Q, then only grad_D), with the bytes it must move.
+    """The backward timed through the plain backward entry point, with the
+    bytes it must move: both gradients in one call (with fp32 gradients the
+    one launch the training step runs, "grad_qd"), and each gradient alone
+    (the entry point called with only grad_Q, then only grad_D).
 
     grad_Q gathers one document row per (pair, query token) hit; grad_D
     zero-fills grad_D (fp32 gradients) and adds one Q row per hit into it.
@@ -453,7 +468,19 @@ def backward_roofline(st: Step, args, stream, flush, peaks) -> dict:
           if not st.same_dtype else "hbm (grad_D write)"}
     gd["l2_gbs"] = gd["l2_bytes"] / (ms_d * 1e-3) / 1e9
     gd["frac"] = gd["achieved"] / gd["peak"]
-    return {"grad_q": gq, "grad_d": gd}
+    out = {"grad_q": gq, "grad_d": gd}
+    if st.fused_bwd:
+        ms_qd = time_it(st.gQ, st.gD)
+        qd_dram = am_bytes + g_bytes + st.gQ.numel() * gel + min(gathered, d_bytes) + i.Q.numel() * el + gd_out
+        out["grad_qd"] = {
+            "kernel": "grad_qd_vec_kernel (after a zero-fill of grad_D, which the one-call step's forward does)",
+            "ms": ms_qd, "hits": hits, "l2_bytes": gathered + red_bytes, "gathered_bytes": gathered,
+            "reduction_bytes": red_bytes, "reductions": hits * (w.dim // 4), "dram_bytes": qd_dram,
+            "l2_gbs": (gathered + red_bytes) / (ms_qd * 1e-3) / 1e9,
+            "achieved": qd_dram / (ms_qd * 1e-3) / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "bound": "l2 (gathers and 16-byte fp32 reductions)" if resident else "hbm"}
+        out["grad_qd"]["frac"] = out["grad_qd"]["achieved"] / out["grad_qd"]["peak"]
+    return out
 
 
 def has_ce_head(name: str) -> bool:
@@ -524,8 +551,8 @@ def run_ours(args):
         "workload": name, "layout": w.layout,
         "Q": list(w.q_shape), "D": list(w.d_shape), "passes": "fwd+bwd" if w.backward else "fwd",
         "grad_dtype": ("input" if st.same_dtype else "f32") if w.backward else None,
-        "loss_head": ("cross-entropy inside the step (one call; the head runs in the backward's "
-                      "first launch)") if st.ce else "score gradient precomputed",
+        "loss_head": ("cross-entropy inside the step (one call; the head runs inside the backward "
+                      "launch)") if st.ce else "score gradient precomputed",
         "argmax": ("recomputed in the backward" if st.recompute else "saved by the forward")
                   if w.backward else None,
         "counted_flops_per_step": w.counted_flops, "valid_token_flops_per_step": st.valid_flops(),

@@ -33,7 +33,11 @@
  *     grad_D[d,j,:] = sum over (q,i) with argmax[q,d,i] == j of g[q,d] * Q[q,i,:]
  * Entries with argmax -1 contribute nothing, so grad_out of an empty
  * document is ignored.  The backward reads the masks only through the
- * argmax that the forward saved.
+ * argmax that the forward saved.  grad_Q is summed in a fixed order.  An
+ * fp32 grad_D is zero-filled and then receives every hit as an fp32 atomic
+ * addition, so its last bits can change from run to run.  With both fp32
+ * gradients requested, dim % 8 == 0 and dim <= 256, a single launch writes
+ * both; otherwise each gradient takes its own launch.
  *
  * Memory, ownership, streams:
  *   - Every pointer is a device pointer (cudaMalloc or managed memory) of
@@ -376,12 +380,15 @@ lik_status lik_ce_rows(const float* scores, int64_t rows, int64_t cols, const in
  *
  * The results are those of the three calls in that order; the launches
  * differ.  When grad_Q and grad_D are both given, dim % 8 == 0, dim <= 256
- * and rows * cols <= 2^20, the loss head runs inside the backward: the
- * grad_Q kernel computes each row's log-sum-exp, row_loss and grad_scores
- * before it uses them, and the grad_D kernel's first block writes *loss (the
- * same fixed-order mean).  With fp32 gradients and the fp16/bf16 all-pairs
- * forward, the forward also zero-fills grad_D (16-byte aligned, element
- * count a multiple of 4) on its producer warp instead of a separate memset.
+ * and rows * cols <= 2^20, the loss head runs inside the backward.  With fp32
+ * gradients and at most 4096 rows the backward is one launch: its blocks
+ * compute their row's log-sum-exp and grad_scores before they use them, and
+ * one more block writes row_loss and *loss (the same fixed-order mean).
+ * Otherwise the grad_Q launch computes the log-sum-exp, row_loss and
+ * grad_scores, and the grad_D launch's first block writes *loss.  With fp32
+ * gradients and the fp16/bf16 all-pairs forward, the forward also zero-fills
+ * grad_D (16-byte aligned, element count a multiple of 4) on its producer
+ * warp instead of a separate memset.
  */
 lik_status lik_maxsim_allpairs_ce_step(const void* Q, const void* D, lik_dtype dtype, int64_t Nq,
                                        int64_t Nd, int64_t Lq, int64_t Ld, int64_t dim,

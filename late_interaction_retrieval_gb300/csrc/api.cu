@@ -284,6 +284,14 @@ lik_status run_bwd(const Problem& P, const float* grad_out, const int32_t* argma
     if ((st = check_aligned(grad_Q, 16, "grad_Q")) != LIK_OK) return st;
     if ((st = check_aligned(grad_D, 16, "grad_D")) != LIK_OK) return st;
     cudaError_t e;
+    if (grad_Q && grad_D && bwd_qd_fusable(P, ce != nullptr)) {  // one launch for both gradients
+        e = ce ? launch_bwd_qd(P, nullptr, argmax, grad_Q, grad_D, ce->scores, ce->target, ce->scale,
+                               ce->row_loss, const_cast<float*>(grad_out), stream)
+               : launch_bwd_qd(P, grad_out, argmax, grad_Q, grad_D, nullptr, nullptr, 0.0f, nullptr, nullptr,
+                               stream);
+        if (e != cudaSuccess) return cuda_fail(e, "backward launch (grad_Q and grad_D)");
+        return LIK_OK;
+    }
     if (ce) {
         e = launch_bwd_grad_q_ce(P, ce->scores, ce->target, ce->scale, ce->row_loss,
                                  const_cast<float*>(grad_out), argmax, grad_Q, false, stream);

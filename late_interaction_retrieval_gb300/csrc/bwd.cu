@@ -15,6 +15,12 @@
 // backward's memory is the two input gradients and nothing else).  Every saved argmax is
 // checked: an index >= Ld is skipped (never dereferenced) and flagged in the
 // library's error word.
+//
+// Kernels: with both gradients in fp32 one launch writes the two
+// (grad_qd_vec_kernel); a gradient requested alone, or gradients in the
+// inputs' 16-bit dtype, take a launch each.  All of them are bound by L2:
+// the gathers read document rows resident there, and the fp32 grad_D
+// reductions are 16-byte read-modify-writes of L2 lines.
 #include "dtype_load.cuh"
 #include "lik_internal.h"
 
@@ -110,15 +116,36 @@ __device__ __forceinline__ void ce_loss_mean(const Problem& P) {
     if (threadIdx.x == 0) *P.ce_loss = acc / static_cast<float>(P.n_query);
 }
 
-// Log-sum-exp of the logits scale * s[0, cols) (one warp; every lane gets it),
-// reduced in a fixed order.
+// Log-sum-exp of the logits scale * s[row, 0:cols) for R rows at once (one
+// warp; every lane gets them), each row reduced in the same fixed order: lane
+// l takes columns l, l + 32, ..., then a butterfly.  The rows' loads are
+// independent, so R rows cost about one row's latency.
+template <int R>
+__device__ __forceinline__ void ce_rows_lse(const float* s, const int64_t (&row)[R], int64_t cols, float scale,
+                                            int lane, float (&lse)[R]) {
+    float m[R], sum[R];
+#pragma unroll
+    for (int k = 0; k < R; ++k) m[k] = -INFINITY;
+    for (int64_t c = lane; c < cols; c += 32)
+#pragma unroll
+        for (int k = 0; k < R; ++k) m[k] = fmaxf(m[k], scale * s[row[k] * cols + c]);
+#pragma unroll
+    for (int k = 0; k < R; ++k) {
+        m[k] = warp_max_f(m[k]);
+        sum[k] = 0.0f;
+    }
+    for (int64_t c = lane; c < cols; c += 32)
+#pragma unroll
+        for (int k = 0; k < R; ++k) sum[k] += expf(scale * s[row[k] * cols + c] - m[k]);
+#pragma unroll
+    for (int k = 0; k < R; ++k) lse[k] = m[k] + logf(warp_sum_f(sum[k]));
+}
+
 __device__ __forceinline__ float ce_row_lse(const float* s, int64_t cols, float scale, int lane) {
-    float m = -INFINITY;
-    for (int64_t c = lane; c < cols; c += 32) m = fmaxf(m, scale * s[c]);
-    m = warp_max_f(m);
-    float sum = 0.0f;
-    for (int64_t c = lane; c < cols; c += 32) sum += expf(scale * s[c] - m);
-    return m + logf(warp_sum_f(sum));
+    const int64_t row[1] = {0};
+    float lse[1];
+    ce_rows_lse<1>(s, row, cols, scale, lane, lse);
+    return lse[0];
 }
 
 // Softmax cross-entropy over the score rows, computed by the grad_Q gather
@@ -403,6 +430,207 @@ grad_d_scatter_atomic_kernel(Problem P, const float* __restrict__ g,
         const T* qrow = Q + (P.query_of(p) * P.Lq + i) * P.dim;
         float* out = gD + (P.doc_of(p) * P.Ld + a) * P.dim;
         for (int64_t k = lane; k < P.dim; k += 32) atomicAdd(out + k, gv * load_f32(qrow + k));
+    }
+}
+
+// ------------------------------------------- grad_Q and grad_D in one pass --
+//
+// Both gradients in fp32, dim % 8 == 0, dim <= 256: one launch does the two.
+// Its CTAs are those of grad_q_vec_kernel (one per query and 16 of its
+// tokens, the query's pairs visited in the same order), so grad_Q is the same
+// fixed-order sum.  The thread that gathers its share of the row D[d, a] for
+// a hit (pair, token i, a = argmax) also adds its share of g * Q[q, i, :]
+// into grad_D[d, a, :] with 16-byte reductions.  That share of Q[q, i, :]
+// (4 consecutive elements in every 32, so that the 8 threads of a row cover
+// 128 contiguous bytes per reduction) is loaded once into registers: the
+// scatter reads nothing per hit, and its reductions are issued while the
+// gathers are in flight.  grad_D must be zero on entry.
+//
+// With the loss head (kCE) every work CTA takes its query row's log-sum-exp
+// for the score gradient, as grad_q_vec_kernel does, and one more CTA, the
+// last, writes every row's loss and their mean (summed as in ce_loss_mean).
+
+constexpr int kLossRows = 4;       // score rows per warp and step in the loss CTA
+constexpr int64_t kFusedLossMaxRows = 4096;
+
+// The rows' losses and their mean (one CTA of kVecThreads threads).
+__device__ __forceinline__ void ce_losses_and_mean(const Problem& P, const CeHead& ce) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t rows = P.n_query, cols = P.pairs_per_query;
+    for (int64_t r0 = static_cast<int64_t>(warp) * kLossRows; r0 < rows; r0 += (kVecThreads / 32) * kLossRows) {
+        int64_t row[kLossRows];
+        float lse[kLossRows];
+#pragma unroll
+        for (int k = 0; k < kLossRows; ++k) row[k] = r0 + k < rows ? r0 + k : rows - 1;
+        ce_rows_lse<kLossRows>(ce.scores, row, cols, ce.scale, lane, lse);
+        if (lane < kLossRows && r0 + lane < rows) {
+            float l = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kLossRows; ++k) if (k == lane) l = lse[k];
+            const int64_t r = r0 + lane;
+            const int32_t t = ce.target[r];
+            ce.row_loss[r] = (t >= 0 && t < cols) ? l - ce.scale * ce.scores[r * cols + t] : 0.0f;
+        }
+    }
+    __syncthreads();  // the row losses written above are visible to the whole CTA
+    if (warp != 0) return;
+    float acc = 0.0f;
+    for (int64_t r = lane; r < rows; r += 32) acc += ce.row_loss[r];
+    acc = warp_sum_f(acc);
+    if (lane == 0) *P.ce_loss = acc / static_cast<float>(rows);
+}
+
+// A 16-byte reduction with no compiler memory barrier: the kernel below never
+// reads grad_D, so its loads need no ordering against these adds.
+__device__ __forceinline__ void red_add_v4_unordered(float* addr, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d));
+}
+
+template <typename T, int VECS, int kUnroll, bool kCE>
+__global__ void __launch_bounds__(kVecThreads, 2)
+grad_qd_vec_kernel(Problem P, const float* __restrict__ g, const int32_t* __restrict__ am,
+                   float* __restrict__ gQ, float* __restrict__ gD, unsigned int* err, CeHead ce) {
+    constexpr int kRedVecs = VECS * 2;  // 4-element pieces of Q per thread: dim <= kRedVecs * 32
+    __shared__ int s_am[kPairChunk][kRowsPerCta];
+    __shared__ float s_g[kPairChunk];
+    __shared__ float s_part[kRowsPerCta][VECS * kThreadsPerRow * kVec];
+    __shared__ float s_lse;
+    __shared__ int s_t;
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    if constexpr (kCE) {
+        if (blockIdx.x == P.n_query * groups) {
+            ce_losses_and_mean(P, ce);
+            return;
+        }
+    }
+    const T* D = static_cast<const T*>(P.D);
+    const T* Q = static_cast<const T*>(P.Q);
+    const int64_t q = blockIdx.x / groups;
+    const int64_t i0 = (blockIdx.x - q * groups) * kRowsPerCta;
+    const int64_t cols = P.pairs_per_query;
+    const float inv_rows = 1.0f / static_cast<float>(P.n_query);
+    const int pg = threadIdx.x / (kRowsPerCta * kThreadsPerRow);  // pair group
+    const int tl = threadIdx.x % (kRowsPerCta * kThreadsPerRow);
+    const int r = tl / kThreadsPerRow, sub = tl % kThreadsPerRow;
+    const int rows_here = static_cast<int>(P.Lq - i0 < kRowsPerCta ? P.Lq - i0 : kRowsPerCta);
+
+    float acc[VECS][kVec];
+#pragma unroll
+    for (int m = 0; m < VECS; ++m)
+#pragma unroll
+        for (int t = 0; t < kVec; ++t) acc[m][t] = 0.f;
+    // this thread's share of Q[q, i0 + r, :] for the scatter
+    float qv[kRedVecs][4];
+#pragma unroll
+    for (int j = 0; j < kRedVecs; ++j) {
+        const int64_t k = static_cast<int64_t>(j) * 32 + sub * 4;
+        if (r < rows_here && k < P.dim)
+            load4(Q + (q * P.Lq + i0 + r) * P.dim + k, qv[j]);
+        else
+            qv[j][0] = qv[j][1] = qv[j][2] = qv[j][3] = 0.f;
+    }
+
+    const int64_t p0 = q * P.pairs_per_query;
+    bool bad = false;
+    for (int64_t c0 = 0; c0 < P.pairs_per_query; c0 += kPairChunk) {
+        const int nc = static_cast<int>(P.pairs_per_query - c0 < kPairChunk ? P.pairs_per_query - c0 : kPairChunk);
+        __syncthreads();
+        const int stage_lo = (kCE && c0 == 0) ? 32 : 0;
+        if (static_cast<int>(threadIdx.x) >= stage_lo) {
+            for (int e = threadIdx.x - stage_lo; e < nc * kRowsPerCta; e += kVecThreads - stage_lo) {
+                const int t = e / kRowsPerCta, rr = e % kRowsPerCta;
+                s_am[t][rr] = rr < rows_here ? am[(p0 + c0 + t) * P.Lq + i0 + rr] : -1;
+            }
+        } else if constexpr (kCE) {
+            const int lane = threadIdx.x & 31;
+            const float lse = ce_row_lse(ce.scores + q * cols, cols, ce.scale, lane);
+            if (lane == 0) {
+                s_lse = lse;
+                s_t = ce.target[q];
+            }
+        }
+        if constexpr (kCE) {
+            if (c0 == 0) __syncthreads();  // s_lse, s_t
+            const float lse = s_lse;
+            const int32_t tq = s_t;
+            const bool row_in = tq >= 0 && tq < cols;
+            for (int t = threadIdx.x; t < nc; t += kVecThreads) {
+                const int64_t c = c0 + t;
+                const float gv = row_in ? ce.scale * (expf(ce.scale * ce.scores[q * cols + c] - lse) -
+                                                      (c == tq ? 1.0f : 0.0f)) * inv_rows
+                                        : 0.0f;
+                s_g[t] = gv;
+                if (i0 == 0) ce.grad[q * cols + c] = gv;
+            }
+        } else {
+            for (int t = threadIdx.x; t < nc; t += kVecThreads) s_g[t] = g[p0 + c0 + t];
+        }
+        __syncthreads();
+        if (r >= rows_here) continue;
+        for (int t = pg; t < nc; t += kUnroll * kPairGroups) {
+            int64_t off[kUnroll];  // element offset of row (d, a) in D and grad_D; -1: no hit
+            float gv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int tt = t + u * kPairGroups;
+                int a = tt < nc ? s_am[tt][r] : -1;
+                if (a >= P.Ld) {
+                    bad = true;
+                    a = -1;
+                }
+                gv[u] = a >= 0 ? s_g[tt] : 0.f;
+                off[u] = a >= 0 ? (P.doc_of_query_pair(q, c0 + tt) * P.Ld + a) * P.dim : -1;
+            }
+#pragma unroll
+            for (int m = 0; m < VECS; ++m) {
+                const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
+                const bool k_in = k < P.dim;
+                Raw8<T> x[kUnroll];
+                if (k_in)
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u)
+                        if (off[u] >= 0) x[u].load(D + off[u] + k);
+                // a share of the scatter (its own range of elements), while the loads are in flight
+#pragma unroll
+                for (int jj = 0; jj < kRedVecs / VECS; ++jj) {
+                    const int j = m * (kRedVecs / VECS) + jj;
+                    const int64_t kr = static_cast<int64_t>(j) * 32 + sub * 4;
+                    if (kr < P.dim) {
+#pragma unroll
+                        for (int u = 0; u < kUnroll; ++u)
+                            if (off[u] >= 0)
+                                red_add_v4_unordered(gD + off[u] + kr, gv[u] * qv[j][0], gv[u] * qv[j][1],
+                                                     gv[u] * qv[j][2], gv[u] * qv[j][3]);
+                    }
+                }
+                if (k_in)
+#pragma unroll
+                    for (int u = 0; u < kUnroll; ++u)
+                        if (off[u] >= 0)
+#pragma unroll
+                            for (int e = 0; e < kVec; ++e) acc[m][e] = fmaf(gv[u], x[u].get(e), acc[m][e]);
+            }
+        }
+    }
+    if (bad) atomicOr(err, kErrBadIndex);
+    __syncthreads();
+    if (pg == 1 && r < rows_here) {
+#pragma unroll
+        for (int m = 0; m < VECS; ++m)
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) s_part[r][(m * kThreadsPerRow + sub) * kVec + e] = acc[m][e];
+    }
+    __syncthreads();
+    if (pg == 1 || r >= rows_here) return;
+    float* out = gQ + (q * P.Lq + i0 + r) * P.dim;
+#pragma unroll
+    for (int m = 0; m < VECS; ++m) {
+        const int64_t k = static_cast<int64_t>(m * kThreadsPerRow + sub) * kVec;
+        if (k >= P.dim) break;
+        float o[kVec];
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) o[e] = acc[m][e] + s_part[r][k + e];
+        store8(out + k, o);
     }
 }
 
@@ -773,6 +1001,29 @@ cudaError_t grad_q_ce_typed(const Problem& P, const CeHead& ce, const int32_t* a
 }
 
 template <typename T>
+cudaError_t grad_qd_typed(const Problem& P, const float* g, const int32_t* am, float* gQ, float* gD,
+                          const CeHead* ce, cudaStream_t stream, unsigned int* err) {
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    const unsigned blocks = static_cast<unsigned>(P.n_query * groups + (ce ? 1 : 0));
+    // rows in flight per thread: as many as 128 registers hold (fp32 rows take twice the registers)
+    constexpr int kU = sizeof(T) == 4 ? 4 : 8;
+    if (ce) {
+        if (P.dim <= 128)
+            grad_qd_vec_kernel<T, 2, kU, true><<<blocks, kVecThreads, 0, stream>>>(P, nullptr, am, gQ, gD, err, *ce);
+        else
+            grad_qd_vec_kernel<T, 4, kU / 2, true><<<blocks, kVecThreads, 0, stream>>>(P, nullptr, am, gQ, gD, err,
+                                                                                    *ce);
+    } else {
+        if (P.dim <= 128)
+            grad_qd_vec_kernel<T, 2, kU, false><<<blocks, kVecThreads, 0, stream>>>(P, g, am, gQ, gD, err, CeHead());
+        else
+            grad_qd_vec_kernel<T, 4, kU / 2, false><<<blocks, kVecThreads, 0, stream>>>(P, g, am, gQ, gD, err,
+                                                                                     CeHead());
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
 cudaError_t grad_d_typed(const Problem& P, const float* g, const int32_t* am, float* gD,
                          cudaStream_t stream, unsigned int* err) {
     const int64_t hits = P.n_pairs * P.Lq;
@@ -793,6 +1044,31 @@ cudaError_t launch_bwd_grad_q(const Problem& P, const float* g, const int32_t* a
     case kF32: return grad_q_typed<float, float>(P, g, am, gQ, stream, err);
     case kF16: return grad_q_typed<__half, float>(P, g, am, gQ, stream, err);
     default: return grad_q_typed<__nv_bfloat16, float>(P, g, am, gQ, stream, err);
+    }
+}
+
+bool bwd_qd_fusable(const Problem& P, bool ce) {
+    const int64_t groups = (P.Lq + kRowsPerCta - 1) / kRowsPerCta;
+    if (!(P.Lq >= 1 && P.n_query >= 1 && P.pairs_per_query >= 1 && P.n_doc * P.Ld * P.dim > 0 &&
+          P.dim % kVec == 0 && P.dim <= 256 && P.n_query * groups < (int64_t(1) << 31) - 1))
+        return false;
+    return !ce || (grad_q_ce_fusable(P) && P.n_query <= kFusedLossMaxRows && P.ce_loss != nullptr);
+}
+
+cudaError_t launch_bwd_qd(const Problem& P, const float* g, const int32_t* am, float* gQ, float* gD,
+                          const float* scores, const int32_t* target, float scale, float* row_loss,
+                          float* grad_scores, cudaStream_t stream) {
+    if (!P.grad_d_zeroed) {  // else the forward of the same step has zero-filled it
+        const cudaError_t e = cudaMemsetAsync(gD, 0, sizeof(float) * P.n_doc * P.Ld * P.dim, stream);
+        if (e != cudaSuccess) return e;
+    }
+    unsigned int* err = device_error_word();
+    const CeHead head{scores, target, scale, row_loss, grad_scores};
+    const CeHead* ce = scores ? &head : nullptr;
+    switch (P.dtype) {
+    case kF32: return grad_qd_typed<float>(P, g, am, gQ, gD, ce, stream, err);
+    case kF16: return grad_qd_typed<__half>(P, g, am, gQ, gD, ce, stream, err);
+    default: return grad_qd_typed<__nv_bfloat16>(P, g, am, gQ, gD, ce, stream, err);
     }
 }
 

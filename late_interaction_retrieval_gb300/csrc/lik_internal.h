@@ -107,6 +107,18 @@ cudaError_t launch_bwd_grad_q(const Problem& P, const float* grad_out,
 cudaError_t launch_bwd_grad_d(const Problem& P, const float* grad_out,
                               const int32_t* argmax, float* grad_D, cudaStream_t stream);
 
+// Both fp32 gradients in one launch (grad_D zero-filled first unless
+// Problem::grad_d_zeroed): the grad_Q gather also scatters each hit into
+// grad_D.  With scores != nullptr the cross-entropy head over the score rows
+// runs inside it (g is then not read: grad_scores is written, with row_loss
+// and *Problem::ce_loss).  Needs Lq >= 1, pairs_per_query >= 1, dim % 8 == 0,
+// dim <= 256; with the head also grad_q_ce_fusable, at most 4096 rows and
+// Problem::ce_loss set.
+bool bwd_qd_fusable(const Problem& P, bool ce);
+cudaError_t launch_bwd_qd(const Problem& P, const float* grad_out, const int32_t* argmax, float* grad_Q,
+                          float* grad_D, const float* scores, const int32_t* target, float scale, float* row_loss,
+                          float* grad_scores, cudaStream_t stream);
+
 // Backward with gradients in the inputs' 16-bit dtype: fp32 sums, one rounded
 // write per element, no zero-fill.  fp16/bf16, dim % 8 == 0, dim <= 256.
 bool bwd_same_dtype_supported(const Problem& P);

@@ -88,18 +88,20 @@ class Layout:
         binding.lik_check_device_error()
         return scores.cpu().numpy(), None if am is None else am.cpu().numpy()
 
-    def gpu_bwd(self, grad_out, argmax, device="cuda"):
+    def gpu_bwd(self, grad_out, argmax, device="cuda", with_q=True, with_d=True):
+        """fp32 gradients from the plain backward entry point (both in one
+        call by default; a gradient not asked for comes back as None)."""
         Q, D, _, _ = self.gpu_inputs(device)
         g = torch.as_tensor(np.ascontiguousarray(grad_out), dtype=torch.float32).to(device)
         am = torch.as_tensor(np.ascontiguousarray(argmax), dtype=torch.int32).to(device)
         shape = self.inp.workload.score_shape
         g = g.reshape(shape)
         am = am.reshape(*shape, self.Lq)
-        gQ = torch.full(Q.shape, float("nan"), dtype=torch.float32, device=device)
-        gD = torch.full(D.shape, float("nan"), dtype=torch.float32, device=device)
+        gQ = torch.full(Q.shape, float("nan"), dtype=torch.float32, device=device) if with_q else None
+        gD = torch.full(D.shape, float("nan"), dtype=torch.float32, device=device) if with_d else None
         getattr(binding, f"lik_maxsim_{self.kind}_bwd")(Q, D, g, am, gQ, gD)
         binding.lik_check_device_error()
-        return gQ.cpu().numpy(), gD.cpu().numpy()
+        return (None if gQ is None else gQ.cpu().numpy()), (None if gD is None else gD.cpu().numpy())
 
     def gpu_bwd_same_dtype(self, grad_out, argmax, device="cuda"):
         """Gradients from the entry points that write them in the inputs' dtype
@@ -147,6 +149,18 @@ class Layout:
         eq = parity.assert_grad_close(gQ_g, gQ_o, tag, "grad_Q")
         ed = parity.assert_grad_close(gD_g, gD_o, tag, "grad_D")
         return dict(grad_q_err=eq, grad_d_err=ed)
+
+    def check_backward_single(self, am_oracle):
+        """Each gradient requested alone (one launch each, not the launch that
+        writes both) against the oracle."""
+        g32 = np.asarray(self.inp.grad_out.cpu().numpy(), np.float32).astype(np.float64)
+        gQ_o, gD_o = self.oracle_bwd(g32, am_oracle)
+        tag = self.inp.workload.dtype
+        gQ_g, none_d = self.gpu_bwd(g32, am_oracle, with_d=False)
+        none_q, gD_g = self.gpu_bwd(g32, am_oracle, with_q=False)
+        assert none_d is None and none_q is None
+        return dict(grad_q_err=parity.assert_grad_close(gQ_g, gQ_o, tag, "grad_Q"),
+                    grad_d_err=parity.assert_grad_close(gD_g, gD_o, tag, "grad_D"))
 
     def check_backward_same_dtype(self, am_oracle):
         """Same-dtype gradients against the oracle: the bar plus one rounding to

@@ -63,7 +63,9 @@ def test_ce_rows_without_gradient_and_empty():
 
 @pytest.mark.parametrize("grads", ["f32", "input"])
 @pytest.mark.parametrize("layout,nq,nd,lq,ld,dim", [("allpairs", 6, 6, 32, 260, 128), ("allpairs", 9, 9, 16, 300, 64),
-                                                    ("kd", 4, 5, 32, 200, 128)])
+                                                    ("kd", 4, 5, 32, 200, 128),
+                                                    # more than 4096 score rows: the head in two backward launches
+                                                    ("kd", 4100, 2, 4, 24, 64)])
 def test_ce_step_matches_oracle(layout, nq, nd, lq, ld, dim, grads):
     inp = separated_case(layout, nq, nd, lq, ld, dim, "bf16", seed=nq * 7 + nd, p_doc_empty=0.0)
     h = gpu_harness.Layout(inp)
@@ -107,8 +109,10 @@ def test_ce_step_matches_oracle(layout, nq, nd, lq, ld, dim, grads):
                                                           ("kd", 3, 6, 12, 70, 32, "f16")])
 def test_ce_step_head_inside_backward(layout, nq, nd, lq, ld, dim, dtype, grads):
     """With both gradients requested, the one-call step computes the loss head
-    inside the backward's launches (row losses and score gradient in the grad_Q
-    gather, their mean in the grad_D launch).  Its loss, row losses and score
+    inside the backward: with fp32 gradients in its one launch (the score
+    gradient in the blocks that use it, the row losses and their mean in one
+    more block), with gradients in the inputs' dtype in the grad_Q launch (the
+    mean in the grad_D launch).  Its loss, row losses and score
     gradient must agree with the separate head (lik_ce_rows) on the step's own
     scores, the loss must be bit-identical from call to call (fixed summation
     order), and the steps without grad_Q or without grad_D (separate head) must

@@ -106,6 +106,30 @@ def test_random_sweep(case, dtype):
     h.check_backward(am_oracle=f["am_oracle"])
 
 
+SINGLE_GRAD_CASES = [
+    # layout,     nq, nd, lq,  ld,  dim
+    ("allpairs",   5,  7, 33,  257, 128),
+    ("allpairs",   3,  4, 32,  300, 256),
+    ("allpairs",   4,  3, 20,   90,  72),
+    ("kd",         3,  5, 32,  260, 128),
+    ("pairwise",   4,  0, 20,  700,  16),
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("case", SINGLE_GRAD_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_single_gradient_calls(case, dtype):
+    """grad_Q alone and grad_D alone (their own launches) against the oracle;
+    the sweep above takes both in the one launch that writes the two."""
+    layout, nq, nd, lq, ld, dim = case
+    inp = random_case(layout, nq, nd, lq, ld, dim, dtype, seed=zlib.crc32(repr(case).encode()) % 10_000,
+                      p_doc_empty=0.15)
+    h = gpu_harness.Layout(inp)
+    f = h.check_forward()
+    h.check_backward_single(am_oracle=f["am_oracle"])
+    h.check_backward(am_oracle=f["am_oracle"])
+
+
 F32_TC_CASES = [
     # layout,     nq, nd, lq,  ld,  dim   (fp32 inputs on the split-TF32 tensor-core kernel)
     ("allpairs",   3,  4,  1,   65,   8),  # one K step, one query token
