@@ -473,7 +473,8 @@ def backward_roofline(st: Step, args, stream, flush, peaks) -> dict:
         ms_qd = time_it(st.gQ, st.gD)
         qd_dram = am_bytes + g_bytes + st.gQ.numel() * gel + min(gathered, d_bytes) + i.Q.numel() * el + gd_out
         out["grad_qd"] = {
-            "kernel": "grad_qd_vec_kernel (after a zero-fill of grad_D, which the one-call step's forward does)",
+            "kernel": "grad_qd_vec_kernel (after a zero-fill of grad_D: a memset here; the forward's side "
+                      "work in the one-call all-pairs step)",
             "ms": ms_qd, "hits": hits, "l2_bytes": gathered + red_bytes, "gathered_bytes": gathered,
             "reduction_bytes": red_bytes, "reductions": hits * (w.dim // 4), "dram_bytes": qd_dram,
             "l2_gbs": (gathered + red_bytes) / (ms_qd * 1e-3) / 1e9,
