@@ -616,7 +616,7 @@ def _twin(st: Step) -> Step:
     return t
 
 
-def run_e2e(st: Step, args, stream, world):
+def run_e2e(st: Step, args, stream, world, nslots: int = 2):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory and reads back its loss (or scores) and
     both gradients.  Two slots of device buffers on three streams, as a
@@ -630,7 +630,7 @@ def run_e2e(st: Step, args, stream, world):
         host["target"] = st.target.cpu().pin_memory()
     elif w.backward:
         host["g"] = st.g.cpu().pin_memory()
-    slots = [st, _twin(st)]
+    slots = [st] + [_twin(st) for _ in range(nslots - 1)]
     dev = [{k: torch.empty_like(v, device=st.device) for k, v in host.items()} for _ in slots]
 
     def outs_of(x: Step):
@@ -645,10 +645,10 @@ def run_e2e(st: Step, args, stream, world):
     ev_in = [torch.cuda.Event() for _ in slots]
     ev_comp = [torch.cuda.Event() for _ in slots]
     ev_out = [torch.cuda.Event() for _ in slots]
-    used = [False, False]
+    used = [False] * nslots
 
     def step_k(k):
-        j = k % 2
+        j = k % nslots
         x, d = slots[j], dev[j]
         if used[j]:
             s_in.wait_event(ev_comp[j])   # the slot's previous step has read its inputs
@@ -696,7 +696,7 @@ def run_e2e(st: Step, args, stream, world):
     # the pipelined steps computed what a plain step computes: the last step's
     # loss (or scores), copied to the host, equals a plain step's bit for bit
     # (both are summed in a fixed order; the inputs are the same)
-    last = back[(k_next[0] - 1) % 2][0]
+    last = back[(k_next[0] - 1) % nslots][0]
     if st.ce:
         st.ce_step()
     else:
@@ -710,7 +710,7 @@ def run_e2e(st: Step, args, stream, world):
         val, unit = whole_job_rate(world, n, w.counted_flops, ms, 1e12), "TFLOP/s"
     return {"value": val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": n, "ms_per_step": ms / n,
-            "pipeline": "2 buffer slots, inputs up / compute / results down on 3 streams"}
+            "pipeline": f"{nslots} buffer slots, inputs up / compute / results down on 3 streams"}
 
 
 # ------------------------------------------------------------- oracle arm --
