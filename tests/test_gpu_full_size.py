@@ -31,11 +31,21 @@ def _gpu_scores_argmax(h, inp):
     return scores, am
 
 
+_ORACLE_FWD = {}
+
+
+def _oracle_fwd(name, h):
+    """The oracle's forward of a full workload (computed once per run)."""
+    if name not in _ORACLE_FWD:
+        _ORACLE_FWD[name] = h.oracle_fwd()
+    return _ORACLE_FWD[name]
+
+
 def _check_full_forward(name):
     inp = generate(name, device="cuda")
     h = gpu_harness.Layout(inp)
     s_g, am_g = _gpu_scores_argmax(h, inp)
-    s_o, am_o, gap = h.oracle_fwd()
+    s_o, am_o, gap = _oracle_fwd(name, h)
     tag = inp.workload.dtype
     parity.assert_scores_close(s_g.cpu().numpy(), s_o, tag)
     Qw = parity.widen(inp.Q)
@@ -88,6 +98,66 @@ def test_kd_b256_n17_bf16_full():
     hit[pairs, am_o.reshape(h.n_pairs, h.Lq)[pairs, toks]] = True
     row_max = np.abs(gD_g.reshape(h.nD, h.Ld, h.dim)).max(axis=2)
     assert not np.any(row_max[~hit])
+
+
+@pytest.mark.parametrize("name", ["inbatch_b128_bf16", "kd_b256_n17_bf16"])
+def test_one_call_step_full(name):
+    """The one-call training step in the launch configuration bench.py times
+    (the forward, the loss head and both fp32 gradients; in-batch, grad_D
+    zero-filled by the forward), at full size.  Scores, argmax, loss and score
+    gradient against the oracle; sampled gradient rows against the oracle
+    backward run on the step's own argmax (each entry checked to be a valid
+    maximum first) with the oracle's score gradient."""
+    inp = generate(name, device="cuda")
+    h = gpu_harness.Layout(inp)
+    rows = h.nQ
+    cols = h.n_pairs // rows
+    dev = inp.Q.device
+    target = inp.ce_target.to(device=dev, dtype=torch.int32).contiguous()
+    scores = torch.empty(rows, cols, device=dev)
+    am = torch.empty(rows, cols, h.Lq, dtype=torch.int32, device=dev)
+    loss = torch.empty(1, device=dev)
+    rl = torch.empty(rows, device=dev)
+    gs = torch.empty(rows, cols, device=dev)
+    gQ = torch.full(inp.Q.shape, float("nan"), device=dev)
+    gD = torch.full(inp.D.shape, float("nan"), device=dev)
+    getattr(binding, f"lik_maxsim_{h.kind}_ce_step")(inp.Q, inp.D, inp.qmask, inp.dmask, target, scores, am, loss,
+                                                     rl, gs, gQ, gD)
+    binding.lik_check_device_error()
+    s_o, am_o, gap = _oracle_fwd(name, h)
+    tag = inp.workload.dtype
+    parity.assert_scores_close(scores.cpu().numpy(), s_o.reshape(rows, cols), tag)
+    am_g = am.cpu().numpy().reshape(h.n_pairs, h.Lq)
+    Qw = parity.widen(inp.Q)
+    Dw = parity.widen(inp.D).reshape(h.nD, h.Ld, h.dim)
+    dm = inp.dmask.cpu().numpy().reshape(h.nD, h.Ld)
+    parity.assert_argmax_valid(am_g, am_o.reshape(h.n_pairs, h.Lq), gap.reshape(h.n_pairs, h.Lq), Qw, Dw,
+                               h.query_of, h.doc_of, dm)
+    loss_o, rl_o, gs_o = oracle.get().ce_rows(s_o.reshape(rows, cols), target.cpu().numpy(), 1.0)
+    assert abs(loss.item() - loss_o) <= parity.TOL[tag] * max(abs(loss_o), 1.0)
+    assert parity.normwise_rel_err(rl.cpu().numpy(), rl_o) <= parity.TOL[tag]
+    assert parity.normwise_rel_err(gs.cpu().numpy(), gs_o) <= parity.TOL[tag]
+    gQ_g, gD_g = gQ.cpu().numpy(), gD.cpu().numpy()
+    assert np.isfinite(gQ_g).all() and np.isfinite(gD_g).all(), "a gradient element was not written"
+    am_g = am_g.reshape(rows, cols, h.Lq)
+    Qn, _ = to_numpy(inp.Q)
+    Dn, _ = to_numpy(inp.D)
+    orc = oracle.get()
+    rng = np.random.default_rng(3)
+    # the GPU's score gradient carries the bf16 bar; the backward is linear in it
+    tol = 2 * parity.TOL[tag]
+    if h.kind == "allpairs":
+        for q in rng.choice(rows, 6, replace=False):
+            gQ_o, _ = orc.allpairs_bwd(Qn[q:q + 1], Dn, gs_o[q:q + 1], am_g[q:q + 1], dtype=tag)
+            assert parity.normwise_rel_err(gQ_g[q], gQ_o[0]) <= tol, f"grad_Q[{q}]"
+        for d in rng.choice(h.nD, 6, replace=False):
+            _, gD_o = orc.allpairs_bwd(Qn, Dn[d:d + 1], gs_o[:, d:d + 1], am_g[:, d:d + 1], dtype=tag)
+            assert parity.normwise_rel_err(gD_g[d], gD_o[0]) <= tol, f"grad_D[{d}]"
+    else:
+        for b in rng.choice(rows, 8, replace=False):
+            gQ_o, gD_o = orc.kd_bwd(Qn[b:b + 1], Dn[b:b + 1], gs_o[b:b + 1], am_g[b:b + 1], dtype=tag)
+            assert parity.normwise_rel_err(gQ_g[b], gQ_o[0]) <= tol, f"grad_Q[{b}]"
+            assert parity.normwise_rel_err(gD_g[b], gD_o[0]) <= tol, f"grad_D[{b}]"
 
 
 def test_rerank_b512_ld8192_f16_full():
