@@ -64,6 +64,9 @@ def test_ce_rows_without_gradient_and_empty():
 @pytest.mark.parametrize("grads", ["f32", "input"])
 @pytest.mark.parametrize("layout,nq,nd,lq,ld,dim", [("allpairs", 6, 6, 32, 260, 128), ("allpairs", 9, 9, 16, 300, 64),
                                                     ("kd", 4, 5, 32, 200, 128),
+                                                    # 4096 score rows: the most the one-launch backward takes,
+                                                    # its loss block summing all of them
+                                                    ("kd", 4096, 2, 4, 24, 64),
                                                     # more than 4096 score rows: the head in two backward launches
                                                     ("kd", 4100, 2, 4, 24, 64)])
 def test_ce_step_matches_oracle(layout, nq, nd, lq, ld, dim, grads):
@@ -154,3 +157,34 @@ def test_ce_step_head_inside_backward(layout, nq, nd, lq, ld, dim, dtype, grads)
     assert parity.normwise_rel_err(d["gQ"].float().cpu().numpy(), a["gQ"].float().cpu().numpy()) <= 1e-5
     for other in (c, d):
         assert abs(other["loss"].item() - a["loss"].item()) <= 1e-6 * max(1.0, abs(a["loss"].item()))
+
+
+def test_one_call_step_repeats_bit_for_bit():
+    """Repeated one-call steps on the same inputs: scores, argmax, loss, row
+    losses, score gradient and grad_Q are bit-identical (fixed summation
+    orders); grad_D, whose hits arrive as fp32 atomic additions, agrees to
+    rounding."""
+    inp = separated_case("allpairs", 12, 12, 32, 420, 128, "bf16", seed=5, p_doc_empty=0.1)
+    h = gpu_harness.Layout(inp)
+    Q, D, qm, dm = h.gpu_inputs()
+    dev = "cuda"
+    rows = cols = 12
+    tt = torch.arange(rows, dtype=torch.int32, device=dev)
+
+    def run():
+        out = dict(scores=torch.empty(rows, cols, device=dev),
+                   am=torch.empty(rows, cols, 32, dtype=torch.int32, device=dev),
+                   loss=torch.empty(1, device=dev), rl=torch.empty(rows, device=dev),
+                   gs=torch.empty(rows, cols, device=dev), gQ=torch.empty(Q.shape, device=dev),
+                   gD=torch.empty(D.shape, device=dev))
+        binding.lik_maxsim_allpairs_ce_step(Q, D, qm, dm, tt, out["scores"], out["am"], out["loss"], out["rl"],
+                                            out["gs"], out["gQ"], out["gD"])
+        binding.lik_check_device_error()
+        return out
+
+    a = run()
+    for _ in range(2):
+        b = run()
+        for k in ("scores", "am", "loss", "rl", "gs", "gQ"):
+            assert torch.equal(a[k], b[k]), k
+        assert parity.normwise_rel_err(b["gD"].cpu().numpy(), a["gD"].cpu().numpy()) <= 1e-6
