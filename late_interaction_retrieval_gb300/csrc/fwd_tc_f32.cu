@@ -46,7 +46,9 @@
 //               (one row per thread), split it and store it into tensor
 //               memory (each warp its lane quarter)
 //   warps 6-9   epilogue: one accumulator row (query token) per thread; a
-//               running (max, argmax) over the valid columns of each tile;
+//               running (max, argmax) over the valid columns of each tile,
+//               read with tcgen05.ld.red (each 16-column unit with its max,
+//               so a fully valid unit needs no ALU work for its max);
 //               at a document's end the valid tokens' maxima are summed per
 //               query in a fixed order and score and argmax written
 // Every mbarrier wait is bounded (ptx::mbar_wait); on expiry the kernel sets
@@ -178,11 +180,22 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
     return d;
 }
 
-// Folds 16 columns (values v, validity bits mw, first column col) into the
-// row's running (max m, argmax am): the unit's max over its valid columns,
-// and, only when it is strictly larger than m, its lowest column.
-__device__ __forceinline__ void fold16(const uint32_t* v, uint32_t mw, int col, float& m, int& am) {
+// Folds 16 columns (values v, validity bits mw, first column col, the load's
+// max of all 16 mred) into the row's running (max m, argmax am): the unit's
+// max over its valid columns (mred when all are valid), and, only when it is
+// strictly larger than m, its lowest column holding it.
+__device__ __forceinline__ void fold16(const uint32_t* v, uint32_t mw, float mred, int col, float& m, int& am) {
     if (mw == 0) return;
+    if (mw == 0xffffu) {  // every column valid: the load's own max
+        if (mred > m) {
+            int idx = 15;
+#pragma unroll
+            for (int c = 14; c >= 0; --c) idx = __uint_as_float(v[c]) == mred ? c : idx;
+            m = mred;
+            am = col + idx;
+        }
+        return;
+    }
     float x[16];
 #pragma unroll
     for (int c = 0; c < 16; ++c) x[c] = ((mw >> c) & 1u) ? __uint_as_float(v[c]) : -FLT_MAX;
@@ -196,6 +209,36 @@ __device__ __forceinline__ void fold16(const uint32_t* v, uint32_t mw, int col, 
         m = um;
         am = col + idx;
     }
+}
+
+// The tile's four 16-column units with their maxima (tcgen05.ld.red, an
+// sm_103a load-with-reduction), one wait for all four.
+__device__ __forceinline__ void tmem_ldmax_16x4(uint32_t ta, uint32_t (&v)[4][16], float (&mx)[4]) {
+    asm volatile(
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, "
+        "%10, %11, %12, %13, %14, %15}, %64, [%68];\n\t"
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, "
+        "%25, %26, %27, %28, %29, %30, %31}, %65, [%69];\n\t"
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, "
+        "%41, %42, %43, %44, %45, %46, %47}, %66, [%70];\n\t"
+        "tcgen05.ld.red.sync.aligned.32x32b.x16.max.f32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, "
+        "%57, %58, %59, %60, %61, %62, %63}, %67, [%71];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(v[0][0]), "=r"(v[0][1]), "=r"(v[0][2]), "=r"(v[0][3]), "=r"(v[0][4]), "=r"(v[0][5]),
+          "=r"(v[0][6]), "=r"(v[0][7]), "=r"(v[0][8]), "=r"(v[0][9]), "=r"(v[0][10]), "=r"(v[0][11]),
+          "=r"(v[0][12]), "=r"(v[0][13]), "=r"(v[0][14]), "=r"(v[0][15]),
+          "=r"(v[1][0]), "=r"(v[1][1]), "=r"(v[1][2]), "=r"(v[1][3]), "=r"(v[1][4]), "=r"(v[1][5]),
+          "=r"(v[1][6]), "=r"(v[1][7]), "=r"(v[1][8]), "=r"(v[1][9]), "=r"(v[1][10]), "=r"(v[1][11]),
+          "=r"(v[1][12]), "=r"(v[1][13]), "=r"(v[1][14]), "=r"(v[1][15]),
+          "=r"(v[2][0]), "=r"(v[2][1]), "=r"(v[2][2]), "=r"(v[2][3]), "=r"(v[2][4]), "=r"(v[2][5]),
+          "=r"(v[2][6]), "=r"(v[2][7]), "=r"(v[2][8]), "=r"(v[2][9]), "=r"(v[2][10]), "=r"(v[2][11]),
+          "=r"(v[2][12]), "=r"(v[2][13]), "=r"(v[2][14]), "=r"(v[2][15]),
+          "=r"(v[3][0]), "=r"(v[3][1]), "=r"(v[3][2]), "=r"(v[3][3]), "=r"(v[3][4]), "=r"(v[3][5]),
+          "=r"(v[3][6]), "=r"(v[3][7]), "=r"(v[3][8]), "=r"(v[3][9]), "=r"(v[3][10]), "=r"(v[3][11]),
+          "=r"(v[3][12]), "=r"(v[3][13]), "=r"(v[3][14]), "=r"(v[3][15]),
+          "=f"(mx[0]), "=f"(mx[1]), "=f"(mx[2]), "=f"(mx[3])
+        : "r"(ta), "r"(ta + 16), "r"(ta + 32), "r"(ta + 48)
+        : "memory");
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -402,19 +445,20 @@ allpairs_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmd, const Params p
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    uint32_t ra[32], rb[32];
+                    uint32_t rv[4][16];
+                    float rmax[4];
                     const uint32_t acc = tmem_base + kAccCol + ab * kT + lane_off;
-                    ptx::tmem_ld_32x2(acc, acc + 32, ra, rb);
+                    tmem_ldmax_16x4(acc, rv, rmax);
                     ptx::tc_fence_before();
                     __syncwarp();
                     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->acc_empty[ab]));
                     if (++ab == kAcc) { ab = 0; aph ^= 1; }
                     // ascending columns, strictly larger wins: the lowest index on ties
                     const int j0 = t * kT;
-                    fold16(ra, mw0 & 0xffffu, j0, m, am);
-                    fold16(ra + 16, mw0 >> 16, j0 + 16, m, am);
-                    fold16(rb, mw1 & 0xffffu, j0 + 32, m, am);
-                    fold16(rb + 16, mw1 >> 16, j0 + 48, m, am);
+                    fold16(rv[0], mw0 & 0xffffu, rmax[0], j0, m, am);
+                    fold16(rv[1], mw0 >> 16, rmax[1], j0 + 16, m, am);
+                    fold16(rv[2], mw1 & 0xffffu, rmax[2], j0 + 32, m, am);
+                    fold16(rv[3], mw1 >> 16, rmax[3], j0 + 48, m, am);
                 }
                 if (!ok) break;
                 // ---- document end: sum each query's valid tokens in a fixed order
