@@ -113,6 +113,8 @@ SINGLE_GRAD_CASES = [
     ("allpairs",   4,  3, 20,   90,  72),
     ("kd",         3,  5, 32,  260, 128),
     ("pairwise",   4,  0, 20,  700,  16),
+    ("allpairs",   3,  5, 16,   70,   8),  # one 8-element vector per row: most threads idle
+    ("allpairs",   2,  3, 24,   90, 136),  # dim 136: four vectors per thread, the last partial
 ]
 
 
