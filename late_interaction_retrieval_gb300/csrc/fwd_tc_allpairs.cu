@@ -26,11 +26,15 @@
 //               warpgroups split each tile's 16-column units round-robin
 //               (unit u goes to group u % 4) and keep a running (max, argmax)
 //               per row; at the end of a document each group hands its
-//               values to the reducer through shared memory
-//               and goes on with the next document.
-//   warp 18     reducer: merges the four groups' values per row, sums each
-//               query's valid rows and writes the score and argmax, while the
-//               epilogue and the MMA continue.
+//               (max, argmax) per row to the reducer through shared memory,
+//               packed into one ordered 64-bit key, and goes on with the
+//               next document.
+//   warp 18     reducer: merges the four groups' keys per row (an unsigned
+//               max), sums each query's valid rows and writes the score and
+//               argmax, while the epilogue and the MMA continue.  It shares
+//               a sub-partition with four epilogue warps, so its instruction
+//               count is on the kernel's critical path: the key merge and,
+//               for 32-token queries, a butterfly sum per query keep it short.
 //   warp 19     MMA issuer of the odd tiles (one issuing thread leaves the
 //               tensor pipe idle while it checks barriers between chains)
 // Lanes 1-31 of the producer warp zero-fill a buffer of the backward that
@@ -117,12 +121,29 @@ struct Bars {
 
 // What the epilogue hands to the reducers at a document's end, per slot.
 struct Exchange {
+    // each warpgroup's (max, column) per accumulator row as one ordered key:
+    // the larger key has the larger max, or the same max and the lower column
+    uint64_t key[kSlots][kEpiGroups][kM];
     int stage_seq[kMaxStages];            // tile (index in the CTA's sequence) each D stage holds
-    float m[kSlots][kEpiGroups][kM];      // each warpgroup's max per accumulator row
-    int a[kSlots][kEpiGroups][kM];        // and its column (-1: none)
-    uint32_t any[kSlots][kEpiGroups][4];  // the warpgroup saw a valid column (per warp quarter)
     float term[kSlots][kM];               // merged per-row terms, summed per query
 };
+
+// (max m, column a) -> key.  m's bits are mapped to an unsigned integer of
+// the same order (-0 taken as +0, so that equal maxima stay equal), and the
+// column is inverted so that the lower column wins a tie; column -1 (none)
+// gives the smallest low word.
+__device__ __forceinline__ uint64_t max_key(float m, int a) {
+    const uint32_t u = __float_as_uint(m + 0.0f);
+    const uint32_t ord = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<uint64_t>(ord) << 32) | (0xffffffffu - static_cast<uint32_t>(a));
+}
+__device__ __forceinline__ float key_max(uint64_t k) {
+    const uint32_t ord = static_cast<uint32_t>(k >> 32);
+    return __uint_as_float((ord & 0x80000000u) ? (ord & 0x7fffffffu) : ~ord);
+}
+__device__ __forceinline__ int key_col(uint64_t k) {
+    return static_cast<int>(0xffffffffu - static_cast<uint32_t>(k));
+}
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float d;
@@ -423,7 +444,6 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         uint32_t best[16];     // that unit's values (masked columns as -FLT_MAX)
 #pragma unroll
         for (int t = 0; t < 16; ++t) best[t] = 0;
-        bool any = false;
         while (ok && cur.valid) {
             uint32_t mw[kUnitsPerGroup / 2];
 #pragma unroll
@@ -433,10 +453,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
             if (cur.t == 0) {
                 m = -INFINITY;
                 bcol = -1;
-                any = false;
             }
-#pragma unroll
-            for (int k = 0; k < kUnitsPerGroup / 2; ++k) any = any || (mw[k] != 0);
 
             // the 16 epilogue warps poll with naps: the MMA issuers, the producer
             // and the reducer share their SM sub-partitions
@@ -483,9 +500,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 ok = ptx::mbar_wait_nap(ptx::smem_u32(&bars->xfree[slot]), xph ^ 1, err, 32);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                xc->m[slot][wg][r] = m;
-                xc->a[slot][wg][r] = am;
-                if (lane == 0) xc->any[slot][wg][quarter] = any ? 1u : 0u;
+                xc->key[slot][wg][r] = max_key(m, am);
                 __syncwarp();  // the warp's writes precede lane 0's arrive (release)
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xfull[slot]));
                 if (++slot == kSlots) { slot = 0; xph ^= 1; }
@@ -497,9 +512,9 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
     } else {
         // ------------------------------------------------------ reducers --
         // Per document: merge the warpgroups' (max, argmax) per row (strictly
-        // greater wins, equal maxima keep the lower column), sum the valid
-        // query tokens' maxima per query in a fixed order, write score and
-        // argmax.  A thread owns rows rr + 32 * kRedWarps * k.
+        // greater wins, equal maxima keep the lower column: the larger key),
+        // sum the valid query tokens' maxima per query in a fixed order,
+        // write score and argmax.  A thread owns rows rr + 32 * kRedWarps * k.
         static_assert(kRedWarps == 1, "the reducer synchronises its lanes with __syncwarp");
         constexpr int kRows = kM / (32 * kRedWarps);
         const int rr = (warp - 2 - kEpiWarps) * 32 + lane;  // the reducer warp(s) follow the epilogue
@@ -550,31 +565,48 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 int am[kRows];
+                float term[kRows];
                 bool any_doc = false;
 #pragma unroll
                 for (int k = 0; k < kRows; ++k) {
                     const int r = rr + k * 32 * kRedWarps;
-                    float mm = xc->m[slot][0][r];
-                    int aa = xc->a[slot][0][r];
-                    bool an = xc->any[slot][0][r >> 5] != 0;
+                    uint64_t kk = xc->key[slot][0][r];
 #pragma unroll
                     for (int g = 1; g < kEpiGroups; ++g) {
-                        const float m1 = xc->m[slot][g][r];
-                        const int a1 = xc->a[slot][g][r];
-                        an = an || xc->any[slot][g][r >> 5] != 0;
-                        if (m1 > mm || (m1 == mm && a1 >= 0 && (aa < 0 || a1 < aa))) {
-                            mm = m1;
-                            aa = a1;
-                        }
+                        const uint64_t k1 = xc->key[slot][g][r];
+                        kk = k1 > kk ? k1 : kk;
                     }
-                    any_doc = an;  // the same for every row: validity is per column
-                    xc->term[slot][r] = (an && qvalid[k]) ? mm : 0.0f;
+                    const float mm = key_max(kk);
+                    const int aa = key_col(kk);
+                    // a row's max is finite exactly when the document has a valid
+                    // column (the same for every row: validity is per column)
+                    const bool an = mm != -INFINITY;
+                    any_doc = an;
+                    term[k] = (an && qvalid[k]) ? mm : 0.0f;
+                    if (Lq != 32) xc->term[slot][r] = term[k];
                     am[k] = (an && qvalid[k]) ? aa : -1;
                 }
                 // the warp's reads of the slot and its term writes are complete:
                 // release the slot, and make the terms visible to the summing lanes
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&bars->xfree[slot]));
+                if (Lq == 32) {
+                    // row lane + 32k is token `lane` of the unit's query k: one
+                    // butterfly per query, every lane ending with the sums
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                        for (int k = 0; k < kRows; ++k) term[k] += __shfl_xor_sync(0xffffffffu, term[k], off);
+#pragma unroll
+                    for (int k = 0; k < kRows; ++k) {
+                        if (!row_ok[k]) continue;
+                        const int64_t pair = q[k] * p.Nd + d;
+                        if (lane == k && p.scores) p.scores[pair] = any_doc ? term[k] : kEmptyDocScore;
+                        if (p.argmax) p.argmax[pair * Lq + lane] = am[k];
+                    }
+                    if (++slot == kSlots) { slot = 0; xph ^= 1; }
+                    continue;
+                }
 #pragma unroll
                 for (int k = 0; k < kRows; ++k) {
                     if (!row_ok[k]) continue;
