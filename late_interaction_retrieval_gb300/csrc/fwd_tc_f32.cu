@@ -463,6 +463,16 @@ allpairs_fwd_tf32_kernel(const __grid_constant__ CUtensorMap tmd, const Params p
                 if (!ok) break;
                 // ---- document end: sum each query's valid tokens in a fixed order
                 const bool live = any && qvalid;
+                if (Lq == 32) {
+                    // the warp's 32 rows are one query's tokens: a butterfly, no exchange
+                    float tsum = live ? m : 0.0f;
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, off);
+                    const int64_t pair = p.layout == kAllPairs ? q * p.Nd + d : d;
+                    if (row_ok && lane == 0 && p.scores) p.scores[pair] = any ? tsum : kEmptyDocScore;
+                    if (row_ok && p.argmax) p.argmax[pair * Lq + iq] = live ? am : -1;
+                    continue;
+                }
                 xc->term[xb][r] = live ? m : 0.0f;
                 // all rows written (bounded wait); the buffer is written again two
                 // documents later, after every thread has passed the next one's wait
