@@ -230,19 +230,17 @@ __device__ __forceinline__ Cursor next_cursor(const Params& p, Cursor c) {
 
 // Mask bytes of this warpgroup's 16-column units of the cursor's tile.
 // Step m covers units wg + 4*(2m) (lanes 0..15) and wg + 4*(2m+1) (lanes
-// 16..31), one column per lane; 0 past the tile or the document.
-__device__ __forceinline__ void prefetch_mask(const Params& p, const Cursor& c, int wg, int lane,
+// 16..31), one column per lane (colb[m], the same in every tile); 0 past the
+// tile or the document.
+__device__ __forceinline__ void prefetch_mask(const Params& p, const Cursor& c, const int (&colb)[kUnitsPerGroup / 2],
                                               uint8_t (&out)[kUnitsPerGroup / 2]) {
-    const uint8_t* dm = p.dmask ? p.dmask + c.d * p.Ld : nullptr;
-    const int lim = c.valid ? static_cast<int>(p.Ld - static_cast<int64_t>(c.t) * p.T) : 0;
     const int jt = c.t * p.T;
+    const uint8_t* dm = p.dmask ? p.dmask + c.d * p.Ld + jt : nullptr;
+    const int rest = static_cast<int>(p.Ld) - jt;
+    const int lim = c.valid ? (rest < p.T ? rest : p.T) : 0;
 #pragma unroll
-    for (int m = 0; m < kUnitsPerGroup / 2; ++m) {
-        const int unit = wg + kEpiGroups * (2 * m + (lane >> 4));
-        const int col = unit * 16 + (lane & 15);
-        const bool in = col < p.T && col < lim;
-        out[m] = in ? (dm ? dm[jt + col] : uint8_t(1)) : uint8_t(0);
-    }
+    for (int m = 0; m < kUnitsPerGroup / 2; ++m)
+        out[m] = colb[m] < lim ? (dm ? dm[colb[m]] : uint8_t(1)) : uint8_t(0);
 }
 
 template <bool kArg>
@@ -438,7 +436,10 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
         // current tile is processed.
         Cursor cur = first_cursor(p), nxt;
         uint8_t pre[kUnitsPerGroup / 2], pre_next[kUnitsPerGroup / 2];
-        prefetch_mask(p, cur, wg, lane, pre);
+        int colb[kUnitsPerGroup / 2];  // this lane's column in each mask step (the same in every tile)
+#pragma unroll
+        for (int m = 0; m < kUnitsPerGroup / 2; ++m) colb[m] = (wg + kEpiGroups * (2 * m + (lane >> 4))) * 16 + (lane & 15);
+        prefetch_mask(p, cur, colb, pre);
         float m = -INFINITY;   // running max of this row over the warpgroup's units
         int bcol = -1;         // first column of the unit that holds m
         uint32_t best[16];     // that unit's values (masked columns as -FLT_MAX)
@@ -449,7 +450,7 @@ allpairs_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_con
 #pragma unroll
             for (int k = 0; k < kUnitsPerGroup / 2; ++k) mw[k] = __ballot_sync(0xffffffffu, pre[k] != 0);
             nxt = next_cursor(p, cur);
-            prefetch_mask(p, nxt, wg, lane, pre_next);
+            prefetch_mask(p, nxt, colb, pre_next);
             if (cur.t == 0) {
                 m = -INFINITY;
                 bcol = -1;
