@@ -74,6 +74,7 @@ SWEEP = [
     ("allpairs",   5,  7, 33,  257,  128),
     ("allpairs",   9,  4, 32, 1030,  128),
     ("allpairs",   2,  3, 128, 300,  128),
+    ("allpairs",   5,  4, 64,  230,  128),  # two 64-token queries per row block
     ("allpairs",  17,  3,  8,   64,   64),
     ("allpairs",   3,  6, 100,  33,  256),
     ("allpairs",   3,  4, 32,  300,  256),  # 80-column tiles: the widest with two D stages at dim 256
